@@ -1,0 +1,281 @@
+"""ctypes binding over libmoeroute's C ABI (include/moe_route.h).
+
+Argument marshalling only: every step of route, dispatch, expert stand-in and
+combine runs in the library's CUDA kernels.  torch supplies device memory and
+streams.  Functions keep the C names without the ``moe_`` prefix; each checks
+shapes, dtypes and devices, allocates outputs that were not passed in (with
+torch, on the input's device), and calls the matching C entry point on the
+current torch stream (or the one given).  A non-OK status raises ``MoeError``.
+
+There is no CPU fallback: if the library is missing, loading raises
+``ImportError``; if the tensors are not on a CUDA device, ``ValueError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+_DTYPE_BF16, _DTYPE_FP8, _DTYPE_FP32 = 0, 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {strerror(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.library_path()
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libmoeroute.so (raises ImportError if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(
+                f"libmoeroute.so not found at {path}; build it with "
+                "`python -m combine_moe_route_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        lib.moe_abi_version.argtypes = []
+        lib.moe_abi_version.restype = i32
+        lib.moe_strerror.argtypes = [i32]
+        lib.moe_strerror.restype = ctypes.c_char_p
+        lib.moe_route_topk.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        lib.moe_route_topk.restype = i32
+        lib.moe_dispatch_workspace_bytes.argtypes = [i32, i32, i32, i64]
+        lib.moe_dispatch_workspace_bytes.restype = sz
+        lib.moe_dispatch.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.moe_dispatch.restype = i32
+        lib.moe_expert_scale.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp]
+        lib.moe_expert_scale.restype = i32
+        lib.moe_combine.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
+        lib.moe_combine.restype = i32
+        lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+        lib.moe_get_device_error.restype = i32
+        _lib = lib
+        return lib
+
+
+def abi_version() -> int:
+    return load_library().moe_abi_version()
+
+
+def strerror(status: int) -> str:
+    return load_library().moe_strerror(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def _stream_handle(stream, device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device}); there is no CPU path")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+# ---------------------------------------------------------------------------
+# route
+# ---------------------------------------------------------------------------
+
+def route_topk(logits: torch.Tensor, K: int, *, topk_idx: torch.Tensor | None = None,
+               topk_w: torch.Tensor | None = None, stream=None):
+    """Top-K experts per token and their softmax weights: (int32 [T,K], fp32 [T,K])."""
+    _dev(logits, "logits", torch.float32)
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T, E]")
+    T, E = logits.shape
+    dev = logits.device
+    if topk_idx is None:
+        topk_idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    _dev(topk_idx, "topk_idx", torch.int32, (T, K))
+    _dev(topk_w, "topk_w", torch.float32, (T, K))
+    with torch.cuda.device(dev):
+        _check(load_library().moe_route_topk(_ptr(logits), T, E, K, _ptr(topk_idx), _ptr(topk_w),
+                                             _stream_handle(stream, dev)), "moe_route_topk")
+    return topk_idx, topk_w
+
+
+# ---------------------------------------------------------------------------
+# dispatch
+# ---------------------------------------------------------------------------
+
+def dispatch_workspace_bytes(R: int, E: int, K: int, T: int) -> int:
+    return int(load_library().moe_dispatch_workspace_bytes(R, E, K, T))
+
+
+@dataclass
+class DispatchResult:
+    recv_x: torch.Tensor            # [T*K, H] bf16 or float8_e4m3fn
+    recv_scale: torch.Tensor | None  # [T*K, H/128] fp32 (FP8 only)
+    counts: torch.Tensor            # [E*R] int32, e-major
+    offsets: torch.Tensor           # [E*R+1] int32
+    expert_offsets: torch.Tensor    # [E+1] int32
+    tok2row: torch.Tensor           # [T*K] int32
+    row2src: torch.Tensor           # [T*K] int32
+    workspace: torch.Tensor         # uint8, holds the device error word
+
+
+def _host_B(B) -> np.ndarray:
+    if isinstance(B, torch.Tensor):
+        if B.device.type != "cpu":
+            raise ValueError("B (tokens per rank) is read on the host: pass a CPU tensor, list or array")
+        B = B.numpy()
+    return np.ascontiguousarray(np.asarray(B, dtype=np.int32))
+
+
+def dispatch(x: torch.Tensor, topk_idx: torch.Tensor, B, E: int, *, fp8: bool = False,
+             out: DispatchResult | None = None, workspace: torch.Tensor | None = None,
+             stream=None) -> DispatchResult:
+    """Count, scan and scatter x [T,H] bf16 into expert-contiguous rows (optionally FP8)."""
+    _dev(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x must be [T, H]")
+    T, H = x.shape
+    _dev(topk_idx, "topk_idx", torch.int32)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != T:
+        raise ValueError("topk_idx must be [T, K]")
+    K = topk_idx.shape[1]
+    Bh = _host_B(B)
+    R = Bh.size
+    if int(Bh.astype(np.int64).sum()) != T:
+        raise ValueError(f"sum(B) = {int(Bh.sum())} does not match x.shape[0] = {T}")
+    dev = x.device
+    rows = T * K
+    if out is None:
+        recv_x = torch.empty((rows, H), dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16, device=dev)
+        recv_scale = torch.empty((rows, H // 128), dtype=torch.float32, device=dev) if fp8 else None
+        out = DispatchResult(
+            recv_x=recv_x, recv_scale=recv_scale,
+            counts=torch.empty(E * R, dtype=torch.int32, device=dev),
+            offsets=torch.empty(E * R + 1, dtype=torch.int32, device=dev),
+            expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            tok2row=torch.empty(rows, dtype=torch.int32, device=dev),
+            row2src=torch.empty(rows, dtype=torch.int32, device=dev),
+            workspace=None)
+    need = dispatch_workspace_bytes(R, E, K, T)
+    if workspace is None:
+        workspace = out.workspace
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    out.workspace = workspace
+    _dev(out.recv_x, "recv_x", (torch.float8_e4m3fn, torch.uint8) if fp8 else torch.bfloat16, (rows, H))
+    if fp8:
+        _dev(out.recv_scale, "recv_scale", torch.float32, (rows, H // 128))
+    for name, n in (("counts", E * R), ("offsets", E * R + 1), ("expert_offsets", E + 1),
+                    ("tok2row", rows), ("row2src", rows)):
+        _dev(getattr(out, name), name, torch.int32, (n,))
+    _dev(workspace, "workspace", torch.uint8)
+    with torch.cuda.device(dev):
+        _check(load_library().moe_dispatch(
+            _ptr(x), _ptr(topk_idx), R, Bh.ctypes.data, E, K, H, _DTYPE_FP8 if fp8 else _DTYPE_BF16,
+            _ptr(out.recv_x), _ptr(out.recv_scale) if fp8 else None, _ptr(out.counts), _ptr(out.offsets),
+            _ptr(out.expert_offsets), _ptr(out.tok2row), _ptr(out.row2src), _ptr(workspace),
+            workspace.numel(), _stream_handle(stream, dev)), "moe_dispatch")
+    return out
+
+
+def get_device_error(workspace: torch.Tensor, stream=None) -> tuple[int, int]:
+    """Synchronise the stream and read the dispatch error word: (status, raw bits)."""
+    _dev(workspace, "workspace", torch.uint8)
+    code = ctypes.c_int32(0)
+    with torch.cuda.device(workspace.device):
+        st = load_library().moe_get_device_error(_ptr(workspace), ctypes.byref(code),
+                                                 _stream_handle(stream, workspace.device))
+    return int(st), int(code.value)
+
+
+# ---------------------------------------------------------------------------
+# expert stand-in and combine
+# ---------------------------------------------------------------------------
+
+def expert_scale(recv_x: torch.Tensor, recv_scale: torch.Tensor | None, expert_offsets: torch.Tensor,
+                 E: int, *, identity: bool = False, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = bf16(xhat * (1 + e/256)) per row of expert e (the grouped-GEMM stand-in)."""
+    fp8 = recv_x.dtype in (torch.float8_e4m3fn, torch.uint8)
+    _dev(recv_x, "recv_x")
+    rows, H = recv_x.shape
+    _dev(expert_offsets, "expert_offsets", torch.int32, (E + 1,))
+    if fp8:
+        _dev(recv_scale, "recv_scale", torch.float32, (rows, H // 128))
+    if out is None:
+        out = torch.empty((rows, H), dtype=torch.bfloat16, device=recv_x.device)
+    _dev(out, "y", torch.bfloat16, (rows, H))
+    with torch.cuda.device(recv_x.device):
+        _check(load_library().moe_expert_scale(
+            _ptr(recv_x), _ptr(recv_scale) if fp8 else None, _DTYPE_FP8 if fp8 else _DTYPE_BF16,
+            _ptr(expert_offsets), E, H, rows, int(bool(identity)), _ptr(out),
+            _stream_handle(stream, recv_x.device)), "moe_expert_scale")
+    return out
+
+
+def combine(y: torch.Tensor, tok2row: torch.Tensor, topk_w: torch.Tensor, *,
+            out_dtype: torch.dtype = torch.bfloat16, out: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    """out[g] = sum_j topk_w[g,j] * y[tok2row[g*K+j]] (fp32 fma, j ascending) -> [T, H]."""
+    _dev(y, "y", torch.bfloat16)
+    _dev(topk_w, "topk_w", torch.float32)
+    if topk_w.dim() != 2:
+        raise ValueError("topk_w must be [T, K]")
+    T, K = topk_w.shape
+    H = y.shape[1]
+    _dev(tok2row, "tok2row", torch.int32)
+    if tok2row.numel() != T * K:
+        raise ValueError("tok2row must have T*K entries")
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype must be bfloat16 or float32")
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=y.device)
+    _dev(out, "out", out_dtype, (T, H))
+    with torch.cuda.device(y.device):
+        _check(load_library().moe_combine(
+            _ptr(y), _ptr(tok2row), _ptr(topk_w), T, K, H,
+            _DTYPE_FP32 if out_dtype == torch.float32 else _DTYPE_BF16, _ptr(out),
+            _stream_handle(stream, y.device)), "moe_combine")
+    return out
+
+
+def moe_layer(x: torch.Tensor, logits: torch.Tensor, B, E: int, K: int, *, fp8: bool = False,
+              identity: bool = False, out_dtype: torch.dtype = torch.bfloat16, stream=None) -> dict:
+    """One layer on the GPU: route, dispatch, expert stand-in, combine (all enqueued, no sync)."""
+    idx, w = route_topk(logits, K, stream=stream)
+    d = dispatch(x, idx, B, E, fp8=fp8, stream=stream)
+    y = expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E, identity=identity, stream=stream)
+    o = combine(y, d.tok2row, w, out_dtype=out_dtype, stream=stream)
+    return dict(topk_idx=idx, topk_w=w, dispatch=d, y=y, out=o)

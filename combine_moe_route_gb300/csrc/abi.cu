@@ -1,0 +1,149 @@
+// abi.cu -- the extern "C" entry points of libmoeroute (declared and
+// documented in include/moe_route.h): host-side argument validation, the
+// per-call rank table, and the kernel launches.  Nothing here allocates,
+// frees or synchronises, except moe_get_device_error, which is documented as
+// synchronous.  Validation runs before the first CUDA call, so a rejected call
+// touches no device state.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "launch.h"
+#include "moe_route.h"
+
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool topk_shape_ok(int E, int K) { return E >= 1 && E <= MOE_MAX_EXPERTS && K >= 1 && K <= E && K <= MOE_MAX_TOPK; }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Fill the rank table from host B; false if any B is negative or T*K overflows int32.
+bool build_rank_table(int R, const int32_t *B, int K, moe::RankTable &rt, long long &T) {
+    memset(&rt, 0, sizeof(rt));
+    rt.R = R;
+    long long acc = 0, tiles = 0;
+    rt.rank_off[0] = 0;
+    rt.tile_off[0] = 0;
+    for (int s = 0; s < R; ++s) {
+        if (B[s] < 0) return false;
+        acc += B[s];
+        if (acc * K >= (1ll << 31)) return false;
+        tiles += ((long long)B[s] * K + moe::kTileItems - 1) / moe::kTileItems;
+        rt.rank_off[s + 1] = (int32_t)acc;
+        rt.tile_off[s + 1] = (int32_t)tiles;
+    }
+    rt.ntiles = (int)tiles;
+    T = acc;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ROUTE_ABI_VERSION; }
+
+const char *moe_strerror(int status) {
+    switch (status) {
+        case MOE_OK: return "success";
+        case MOE_ERR_INVALID_ARG: return "invalid argument (NULL pointer, size out of range or inconsistent shape)";
+        case MOE_ERR_UNSUPPORTED: return "unsupported argument (pointer not 16-byte aligned)";
+        case MOE_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+        case MOE_ERR_WORKSPACE: return "workspace missing or smaller than moe_dispatch_workspace_bytes()";
+        case MOE_ERR_TIMEOUT: return "a bounded device wait ran out";
+        case MOE_ERR_BAD_ROUTING: return "routing has an expert id out of range or repeated within a token";
+        default: return "unknown moe_status";
+    }
+}
+
+moe_status moe_route_topk(const float *logits, int T, int E, int K, int32_t *topk_idx, float *topk_w,
+                          moe_stream_t stream) {
+    if (T < 0 || !topk_shape_ok(E, K)) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * E >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_route_topk(logits, T, E, K, topk_idx, topk_w, (cudaStream_t)stream));
+}
+
+size_t moe_dispatch_workspace_bytes(int R, int E, int K, int64_t T) {
+    if (R < 1 || R > MOE_MAX_RANKS || !topk_shape_ok(E, K) || E % R != 0) return 0;
+    if (T < 0 || T * K >= (1ll << 31)) return 0;
+    const int ntiles = moe::max_tiles(R, K, T);
+    return moe::plan_dispatch(E, ntiles).total;
+}
+
+moe_status moe_dispatch(const void *x, const int32_t *topk_idx, int R, const int32_t *B, int E, int K, int H,
+                        moe_dtype recv_dtype, void *recv_x, float *recv_scale, int32_t *counts, int32_t *offsets,
+                        int32_t *expert_offsets, int32_t *tok2row, int32_t *row2src, void *workspace,
+                        size_t workspace_bytes, moe_stream_t stream) {
+    if (R < 1 || R > MOE_MAX_RANKS || !B || !topk_shape_ok(E, K) || E % R != 0) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (recv_dtype != MOE_DTYPE_BF16 && recv_dtype != MOE_DTYPE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = recv_dtype == MOE_DTYPE_FP8_E4M3;
+    if (fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
+    moe::RankTable rt;
+    long long T = 0;
+    if (!build_rank_table(R, B, K, rt, T)) return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || !expert_offsets) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E * R, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * ((size_t)E * R + 1), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * ((size_t)E + 1), st);
+        return cuda_status(e);
+    }
+    if (!x || !topk_idx || !recv_x || !tok2row || !row2src || (fp8 && !recv_scale)) return MOE_ERR_INVALID_ARG;
+    if (!workspace) return MOE_ERR_WORKSPACE;
+    const moe::DispatchPlan plan = moe::plan_dispatch(E, rt.ntiles);
+    if (workspace_bytes < plan.total) return MOE_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(recv_x) || !aligned16(workspace) || (fp8 && !aligned16(recv_scale)))
+        return MOE_ERR_UNSUPPORTED;
+    return cuda_status(moe::launch_dispatch(x, topk_idx, rt, E, K, H, fp8, recv_x, fp8 ? recv_scale : nullptr, counts,
+                                            offsets, expert_offsets, tok2row, row2src, workspace, st));
+}
+
+moe_status moe_expert_scale(const void *recv_x, const float *recv_scale, moe_dtype recv_dtype,
+                            const int32_t *expert_offsets, int E, int H, int rows, int identity, void *y,
+                            moe_stream_t stream) {
+    if (E < 1 || E > MOE_MAX_EXPERTS || rows < 0) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (recv_dtype != MOE_DTYPE_BF16 && recv_dtype != MOE_DTYPE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = recv_dtype == MOE_DTYPE_FP8_E4M3;
+    if (fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!recv_x || !expert_offsets || !y || (fp8 && !recv_scale)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(recv_x) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(moe::launch_expert_scale(recv_x, recv_scale, fp8, expert_offsets, E, H, rows, identity, y,
+                                                (cudaStream_t)stream));
+}
+
+moe_status moe_combine(const void *y, const int32_t *tok2row, const float *topk_w, int T, int K, int H,
+                       moe_dtype out_dtype, void *out, moe_stream_t stream) {
+    if (T < 0 || K < 1 || K > MOE_MAX_TOPK) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * K >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+    if (out_dtype != MOE_DTYPE_BF16 && out_dtype != MOE_DTYPE_FP32) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y || !tok2row || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(
+        moe::launch_combine(y, tok2row, topk_w, T, K, H, out_dtype == MOE_DTYPE_FP32, out, (cudaStream_t)stream));
+}
+
+moe_status moe_get_device_error(const void *workspace, int32_t *host_code, moe_stream_t stream) {
+    if (!workspace || !host_code) return MOE_ERR_INVALID_ARG;
+    int32_t v = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    *host_code = v;
+    if (v & (MOE_DEVERR_SCAN_TIMEOUT | MOE_DEVERR_COPY_TIMEOUT)) return MOE_ERR_TIMEOUT;
+    if (v & (MOE_DEVERR_EXPERT_RANGE | MOE_DEVERR_DUPLICATE)) return MOE_ERR_BAD_ROUTING;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+// combine.cu -- gather each token's K expert outputs and take their
+// routing-weighted sum.
+//
+// Sources:
+//  * lehuy.net, "Decoding high-performance EP kernels", "Optimising for
+//    throughput" > "Combine": undo the permutation dispatch applied, bring the
+//    outputs back to their source slots and add up each token's
+//    contributions; the routing dispatch produced is reused, so no
+//    coordination pass is needed.
+//  * Perplexity, "Enabling trillion-parameter models on AWS EFA", "Dispatch
+//    and combine": the combine receiver accumulates the returned tokens into
+//    the output tensors (accumulation on the receiving side).
+//
+// On one GPU the return trip is a gather: token g reads rows tok2row[g*K+j]
+// of y directly.  Each thread owns 16-byte column chunks (8 bf16 channels) of
+// the token's row; for a chunk it issues the K row loads (up to 8 at a time,
+// all in flight together), then folds them into 8 fp32 accumulators with
+// fused multiply-adds in the fixed order j = 0..K-1, and writes bf16 (round
+// to nearest even) or fp32.  The block walks tokens g = blockIdx.x,
+// blockIdx.x + gridDim.x, ...; weights and rows of the token sit in shared
+// memory.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "launch.h"
+
+namespace moe {
+
+constexpr int kCombineThreads = 128;
+constexpr int kCombineBatch = 8;   // row loads in flight per chunk
+
+template <bool kOutF32>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __nv_bfloat16 *__restrict__ y,
+                                                                  const int32_t *__restrict__ tok2row,
+                                                                  const float *__restrict__ topk_w, int T, int K,
+                                                                  int H, void *__restrict__ out) {
+    __shared__ int32_t s_row[MOE_MAX_TOPK];
+    __shared__ float s_w[MOE_MAX_TOPK];
+    const long long rows = (long long)T * K;
+    const int nchunk = H / 8;
+
+    for (long long g = blockIdx.x; g < T; g += gridDim.x) {
+        __syncthreads();   // previous token's readers are done with s_row / s_w
+        if (threadIdx.x < K) {
+            const int r = __ldg(tok2row + g * K + threadIdx.x);
+            s_row[threadIdx.x] = (r >= 0 && r < rows) ? r : -1;
+            s_w[threadIdx.x] = __ldg(topk_w + g * K + threadIdx.x);
+        }
+        __syncthreads();
+
+        for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+            float acc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+            for (int j0 = 0; j0 < K; j0 += kCombineBatch) {
+                uint4 v[kCombineBatch];
+#pragma unroll
+                for (int jj = 0; jj < kCombineBatch; ++jj) {
+                    const int j = j0 + jj;
+                    const int r = (j < K) ? s_row[j] : -1;
+                    v[jj] = (r >= 0) ? ld_stream_v4(y + (size_t)r * H + (size_t)c * 8) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int jj = 0; jj < kCombineBatch; ++jj) {
+                    const int j = j0 + jj;
+                    if (j < K && s_row[j] >= 0) {
+                        const float w = s_w[j];
+                        const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v[jj]);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 f = __bfloat1622float2(h2[k]);
+                            acc[2 * k] = __fmaf_rn(w, f.x, acc[2 * k]);
+                            acc[2 * k + 1] = __fmaf_rn(w, f.y, acc[2 * k + 1]);
+                        }
+                    }
+                }
+            }
+            if (kOutF32) {
+                float *o = static_cast<float *>(out) + (size_t)g * H + (size_t)c * 8;
+                st_v4(o, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                                    __float_as_uint(acc[3])));
+                st_v4(o + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]), __float_as_uint(acc[6]),
+                                        __float_as_uint(acc[7])));
+            } else {
+                uint4 pk;
+                __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) p2[k] = __floats2bfloat162_rn(acc[2 * k], acc[2 * k + 1]);
+                st_v4(static_cast<__nv_bfloat16 *>(out) + (size_t)g * H + (size_t)c * 8, pk);
+            }
+        }
+    }
+}
+
+cudaError_t launch_combine(const void *y, const int32_t *tok2row, const float *topk_w, int T, int K, int H,
+                           bool out_f32, void *out, cudaStream_t stream) {
+    long long grid = (long long)device_sm_count() * 16;
+    if (grid > T) grid = T;
+    if (grid < 1) grid = 1;
+    const __nv_bfloat16 *yb = static_cast<const __nv_bfloat16 *>(y);
+    if (out_f32)
+        combine_kernel<true><<<(unsigned)grid, kCombineThreads, 0, stream>>>(yb, tok2row, topk_w, T, K, H, out);
+    else
+        combine_kernel<false><<<(unsigned)grid, kCombineThreads, 0, stream>>>(yb, tok2row, topk_w, T, K, H, out);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------------------
+// expert stand-in: y[row] = bf16(xhat * s_e), s_e = 1 + e/256 (or 1)
+// --------------------------------------------------------------------------
+// Not one of the sources' kernels: it replaces the grouped expert GEMM so that
+// combine has deterministic, expert-dependent inputs.  One thread per 8
+// channels of a row; the row's expert comes from a binary search over
+// expert_offsets held in shared memory.
+template <bool kFp8>
+__global__ void __launch_bounds__(256) expert_scale_kernel(const void *__restrict__ recv,
+                                                           const float *__restrict__ recv_scale,
+                                                           const int32_t *__restrict__ expert_offsets, int E, int H,
+                                                           int rows, int identity, __nv_bfloat16 *__restrict__ y) {
+    extern __shared__ int32_t s_eo[];   // [E + 1]
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_eo[i] = expert_offsets[i];
+    __syncthreads();
+    const int nchunk = H / 8;
+    const long long total = (long long)rows * nchunk;
+    for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < total;
+         v += (long long)gridDim.x * blockDim.x) {
+        const int row = (int)(v / nchunk);
+        const int c = (int)(v - (long long)row * nchunk);
+        // expert of the row: s_eo[e] <= row < s_eo[e+1]
+        int lo = 0, hi = E;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_eo[mid] <= row) lo = mid; else hi = mid;
+        }
+        const float se = identity ? 1.0f : 1.0f + (float)lo / 256.0f;
+        float f[8];
+        if (kFp8) {
+            const uint2 q = *reinterpret_cast<const uint2 *>(static_cast<const unsigned char *>(recv) +
+                                                             (size_t)row * H + (size_t)c * 8);
+            const float sc = recv_scale[(size_t)row * (H / 128) + (c * 8) / 128];
+            const uint32_t w[2] = {q.x, q.y};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[k >> 1] >> (16 * (k & 1))) & 0xffffu);
+                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+                const float2 fl = __half22float2(__half2(hr));
+                f[2 * k] = __fmul_rn(fl.x, sc);
+                f[2 * k + 1] = __fmul_rn(fl.y, sc);
+            }
+        } else {
+            const uint4 u = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(recv) +
+                                                             (size_t)row * H + (size_t)c * 8);
+            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 t = __bfloat1622float2(h2[k]);
+                f[2 * k] = t.x;
+                f[2 * k + 1] = t.y;
+            }
+        }
+        uint4 pk;
+        __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) p2[k] = __floats2bfloat162_rn(__fmul_rn(f[2 * k], se), __fmul_rn(f[2 * k + 1], se));
+        *reinterpret_cast<uint4 *>(y + (size_t)row * H + (size_t)c * 8) = pk;
+    }
+}
+
+cudaError_t launch_expert_scale(const void *recv, const float *recv_scale, bool fp8, const int32_t *expert_offsets,
+                                int E, int H, int rows, int identity, void *y, cudaStream_t stream) {
+    const long long total = (long long)rows * (H / 8);
+    long long grid = (total + 255) / 256;
+    const long long cap = (long long)device_sm_count() * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    const size_t smem = (size_t)(E + 1) * 4;
+    __nv_bfloat16 *yb = static_cast<__nv_bfloat16 *>(y);
+    if (fp8)
+        expert_scale_kernel<true><<<(unsigned)grid, 256, smem, stream>>>(recv, recv_scale, expert_offsets, E, H, rows,
+                                                                         identity, yb);
+    else
+        expert_scale_kernel<false><<<(unsigned)grid, 256, smem, stream>>>(recv, recv_scale, expert_offsets, E, H,
+                                                                          rows, identity, yb);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

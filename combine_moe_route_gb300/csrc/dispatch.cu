@@ -1,0 +1,584 @@
+// dispatch.cu -- count, exclusive scan and scatter of tokens into the
+// expert-contiguous receive buffer, with an optional fused FP8 quantise.
+//
+// Sources:
+//  * lehuy.net, "Decoding high-performance EP kernels", "Optimising for
+//    throughput: ask first, send later" > "Dispatch": the layout is not known
+//    in advance; count what goes where, exchange the counts, and a prefix sum
+//    over them fixes a conflict-free layout; then each token is copied to the
+//    slot the prefix sum assigned.
+//  * Perplexity, "Enabling trillion-parameter models on AWS EFA", "Dispatch
+//    and combine": per-expert token counts by shared-memory atomics inside a
+//    block, a cumulative sum for the offsets, rows packed contiguously and
+//    reorganised into the grouped-GEMM input.
+//  * Perplexity, "Lower latency and higher throughput with multi-node DeepSeek
+//    deployment", "Quantization": activation scales over 128-element vectors,
+//    computed on the fly.
+//
+// With all R ranks in one HBM the count exchange is a read of the histogram
+// in global memory and the send+receive pair is a single hop: each source row
+// is staged once in shared memory by a bulk copy and written by bulk copies
+// straight into its K destination rows.
+//
+// Three kernels, stream-ordered:
+//  1. tile histogram: the items (g, j) of one rank are cut into tiles of
+//     kTileItems consecutive items.  Each warp counts its run of 256 items
+//     into a warp-private shared histogram; lanes holding the same expert are
+//     grouped with __match_any_sync and their leader adds the group size with
+//     one shared-memory atomic, whose return value plus the lane's position in
+//     the group is the item's rank among equal experts so far.  The warps'
+//     histograms are then combined in warp order, giving every item a stable
+//     rank inside (expert, tile) and every tile its per-expert total.
+//  2. exclusive scan over the histogram laid out expert-major, tile-minor
+//     (e * ntiles + tile), one pass with decoupled lookback.  Because tiles
+//     are rank-major and ranks hold consecutive tokens, this order is exactly
+//     (expert, source rank, token): the scanned value of (e, tile) is the
+//     first receive row of expert e's items in that tile.
+//  3. scatter: row(g, j) = scan[e * ntiles + tile(g, j)] + rank-in-tile;
+//     copy (or quantise once and copy) x[g] into its K rows.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "launch.h"
+
+namespace moe {
+
+// --------------------------------------------------------------------------
+// 1. tile histogram + stable in-tile ranks
+// --------------------------------------------------------------------------
+// local_rank (aliases the tok2row output): in-tile rank of each item, or -1.
+__global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *__restrict__ topk_idx, int E, int K,
+                                                                 const __grid_constant__ RankTable rt,
+                                                                 int32_t *__restrict__ tile_hist,
+                                                                 int32_t *__restrict__ local_rank,
+                                                                 int32_t *__restrict__ err) {
+    extern __shared__ int32_t hist[];   // [kHistWarps][E]
+    const int tile = blockIdx.x;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const int s = upper_bound_minus_one(rt.tile_off, rt.R, tile);
+    const long long rank_lo = (long long)rt.rank_off[s] * K;
+    const long long rank_hi = (long long)rt.rank_off[s + 1] * K;
+    const long long lo = rank_lo + (long long)(tile - rt.tile_off[s]) * kTileItems;
+    const long long hi = min(lo + (long long)kTileItems, rank_hi);
+
+    for (int i = threadIdx.x; i < kHistWarps * E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+
+    int32_t *my_hist = hist + warp * E;
+    const unsigned lanemask_lt = (1u << lane) - 1u;
+    int e_reg[kItemsPerThread];
+    int r_reg[kItemsPerThread];
+    int bad = 0;
+#pragma unroll
+    for (int step = 0; step < kItemsPerThread; ++step) {
+        const long long i = lo + warp * kItemsPerWarp + step * 32 + lane;
+        int e = -1;
+        if (i < hi) {
+            e = __ldg(topk_idx + i);
+            if (e < 0 || e >= E) {
+                bad = 1;
+                e = -1;
+            }
+        }
+        // invalid lanes get distinct negative keys so they never form a group with a valid lane
+        const int key = (e >= 0) ? e : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        int r = -1;
+        if (e >= 0) {
+            const int leader = __ffs(peers) - 1;
+            int base = 0;
+            if (lane == leader) base = atomicAdd(&my_hist[e], __popc(peers));
+            base = __shfl_sync(peers, base, leader);
+            r = base + __popc(peers & lanemask_lt);
+        }
+        e_reg[step] = e;
+        r_reg[step] = r;
+        __syncwarp();
+    }
+    if (bad) set_device_error(err, MOE_DEVERR_EXPERT_RANGE);
+    __syncthreads();
+
+    // combine the warps' histograms in warp order: hist[w][e] becomes the
+    // exclusive prefix over warps, the tile total goes to global memory
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < kHistWarps; ++w) {
+            const int c = hist[w * E + e];
+            hist[w * E + e] = run;
+            run += c;
+        }
+        tile_hist[(long long)e * rt.ntiles + tile] = run;
+    }
+    __syncthreads();
+
+#pragma unroll
+    for (int step = 0; step < kItemsPerThread; ++step) {
+        const long long i = lo + warp * kItemsPerWarp + step * 32 + lane;
+        if (i < hi) {
+            const int e = e_reg[step];
+            local_rank[i] = (e >= 0) ? my_hist[e] + r_reg[step] : -1;
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// 2. exclusive scan with decoupled lookback
+// --------------------------------------------------------------------------
+// status[b]: 0 = not yet published; (1 << 62 | aggregate) = block aggregate;
+// (2 << 62 | inclusive prefix) = everything up to and including block b.
+constexpr unsigned long long kFlagAgg = 1ull << 62;
+constexpr unsigned long long kFlagPrefix = 2ull << 62;
+constexpr unsigned long long kFlagMask = 3ull << 62;
+
+__device__ __forceinline__ int warp_inclusive_scan(int v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += o;
+    }
+    return v;
+}
+
+// out[0..n] = exclusive prefix of in[0..n-1]; out[n] = total.
+__global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32_t *__restrict__ in,
+                                                                     int32_t *__restrict__ out, int n,
+                                                                     unsigned long long *status, int32_t *ticket,
+                                                                     int32_t *err) {
+    __shared__ int s_vid;
+    __shared__ int s_warp[kScanThreads / 32];
+    __shared__ int s_excl;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+
+    // virtual block id in start order: every lower id has started, so the
+    // lookback below only waits on blocks that are already running
+    if (tid == 0) s_vid = atomicAdd(ticket, 1);
+    __syncthreads();
+    const int vid = s_vid;
+    const long long base = (long long)vid * kScanChunk + (long long)tid * kScanPerThread;
+
+    int v[kScanPerThread];
+    int sum = 0;
+#pragma unroll
+    for (int k = 0; k < kScanPerThread; ++k) {
+        v[k] = (base + k < n) ? in[base + k] : 0;
+        sum += v[k];
+    }
+    const int incl = warp_inclusive_scan(sum);
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int wv = (lane < kScanThreads / 32) ? s_warp[lane] : 0;
+        const int wincl = warp_inclusive_scan(wv);
+        if (lane < kScanThreads / 32) s_warp[lane] = wincl - wv;   // exclusive over warps
+        if (lane == kScanThreads / 32 - 1) {
+            const int aggregate = wincl;
+            int excl = 0;
+            if (vid == 0) {
+                __threadfence();
+                atomicExch(&status[0], kFlagPrefix | (unsigned long long)(unsigned)aggregate);
+            } else {
+                atomicExch(&status[vid], kFlagAgg | (unsigned long long)(unsigned)aggregate);
+                int p = vid - 1;
+                const uint64_t t0 = global_timer_ns();
+                bool timed_out = false;
+                while (p >= 0) {
+                    const unsigned long long st = ld_volatile_u64(&status[p]);
+                    const unsigned long long flag = st & kFlagMask;
+                    if (flag == 0ull) {
+                        if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            timed_out = true;
+                            break;
+                        }
+                        __nanosleep(32);
+                        continue;
+                    }
+                    excl += (int)(unsigned)(st & 0xffffffffull);
+                    if (flag == kFlagPrefix) break;
+                    --p;
+                }
+                if (timed_out) set_device_error(err, MOE_DEVERR_SCAN_TIMEOUT);
+                __threadfence();
+                atomicExch(&status[vid], kFlagPrefix | (unsigned long long)(unsigned)(excl + aggregate));
+            }
+            s_excl = excl;
+            if ((long long)(vid + 1) * kScanChunk >= n) out[n] = excl + aggregate;   // last block: total
+        }
+    }
+    __syncthreads();
+    int run = s_excl + s_warp[warp] + (incl - sum);
+#pragma unroll
+    for (int k = 0; k < kScanPerThread; ++k) {
+        if (base + k < n) out[base + k] = run;
+        run += v[k];
+    }
+}
+
+// --------------------------------------------------------------------------
+// 3. scatter (+ fused FP8 quantise)
+// --------------------------------------------------------------------------
+struct ScatterArgs {
+    const __nv_bfloat16 *x;
+    const int32_t *topk_idx;
+    const int32_t *scan;       // [E * ntiles + 1]
+    void *recv_x;
+    float *recv_scale;
+    int32_t *counts;
+    int32_t *offsets;
+    int32_t *expert_offsets;
+    int32_t *tok2row;          // in: in-tile ranks; out: rows
+    int32_t *row2src;
+    int32_t *err;
+    int T, E, K, H;
+    int stages;
+};
+
+// Shared memory per stage: the bf16 source row, then (FP8) the e4m3 row and
+// its H/128 scales, then the K destination rows.
+__host__ __device__ inline size_t scatter_stage_bytes(int H, int K, bool fp8) {
+    size_t b = (size_t)H * 2;
+    if (fp8) b += (size_t)H + (size_t)(H / 128) * 4;
+    b += (size_t)K * 4;
+    return (b + 127) & ~(size_t)127;
+}
+
+// 16 lanes quantise one 128-channel block: lane owns 8 consecutive channels.
+__device__ __forceinline__ void quantize_block16(const uint4 xin, uint2 &qout, float &scale_out) {
+    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&xin);
+    float f[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 t = __bfloat1622float2(h2[k]);
+        f[2 * k] = t.x;
+        f[2 * k + 1] = t.y;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    amax = fmaxf(amax, 0x1p-64f);
+    scale_out = __fdiv_rn(amax, 448.0f);
+    const float inv = __fdiv_rn(448.0f, amax);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float a = __fmul_rn(f[2 * k], inv);
+        const float b = __fmul_rn(f[2 * k + 1], inv);
+        // low byte = first element (little endian, same as consecutive bytes in memory)
+        w[k] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    }
+    qout.x = w[0] | (w[1] << 16);
+    qout.y = w[2] | (w[3] << 16);
+}
+
+// Wait until at most n (0..7) of this thread's committed bulk store groups
+// are still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_dyn(int n) {
+    switch (n) {
+        case 0: bulk_wait_read<0>(); break;
+        case 1: bulk_wait_read<1>(); break;
+        case 2: bulk_wait_read<2>(); break;
+        case 3: bulk_wait_read<3>(); break;
+        case 4: bulk_wait_read<4>(); break;
+        case 5: bulk_wait_read<5>(); break;
+        case 6: bulk_wait_read<6>(); break;
+        default: bulk_wait_read<7>(); break;
+    }
+}
+
+// Persistent over tokens g = blockIdx.x + it * gridDim.x.  Thread 0 drives an
+// S-stage ring of bulk copies: the bf16 source row of token it + S - 1 is in
+// flight while token it is copied out.  bf16: the K destination rows are
+// written by bulk stores straight from the staged source row.  FP8: all
+// threads quantise the staged row once (16 lanes per 128-channel block) into
+// an e4m3 row and its scales in shared memory; the e4m3 row leaves by K bulk
+// stores, the scales by plain coalesced stores.
+template <bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? 256 : 128) scatter_kernel(const ScatterArgs a,
+                                                                    const __grid_constant__ RankTable rt) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full_bar[8];
+
+    const int tid = threadIdx.x;
+    const int S = a.stages;
+    const int H = a.H;
+    const int K = a.K;
+    const int E = a.E;
+    const int nblk = H / 128;
+    const size_t stage_bytes = scatter_stage_bytes(H, K, kFp8);
+    const uint32_t in_bytes = (uint32_t)H * 2u;
+    const uint32_t out_bytes = kFp8 ? (uint32_t)H : in_bytes;
+    const size_t recv_pitch = kFp8 ? (size_t)H : (size_t)H * 2;
+
+    // counts / offsets / expert_offsets from the scanned histogram
+    {
+        const int n = E * rt.R;
+        for (int i = blockIdx.x * blockDim.x + tid; i <= n; i += gridDim.x * blockDim.x) {
+            if (i < n) {
+                const int e = i / rt.R;
+                const int s = i - e * rt.R;
+                const int o = a.scan[(long long)e * rt.ntiles + rt.tile_off[s]];
+                const int o1 = a.scan[(long long)e * rt.ntiles + rt.tile_off[s + 1]];
+                a.offsets[i] = o;
+                a.counts[i] = o1 - o;
+                if (s == 0) a.expert_offsets[e] = o;
+            } else {
+                const int total = a.scan[(long long)E * rt.ntiles];
+                a.offsets[n] = total;
+                a.expert_offsets[E] = total;
+            }
+        }
+    }
+
+    const int T = a.T;
+    if ((int)blockIdx.x >= T) return;
+    const int my_count = (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
+
+    auto stage_in = [&](int st) { return smem + (size_t)st * stage_bytes; };
+    auto stage_q = [&](int st) { return stage_in(st) + (size_t)H * 2; };
+    auto stage_sc = [&](int st) { return reinterpret_cast<float *>(stage_q(st) + H); };
+    auto stage_rows = [&](int st) {
+        return reinterpret_cast<int32_t *>(stage_in(st) + (size_t)H * 2 +
+                                           (kFp8 ? (size_t)H + (size_t)nblk * 4 : 0));
+    };
+    auto token_of = [&](int it) { return (long long)blockIdx.x + (long long)it * gridDim.x; };
+
+    int loads_issued = 0;   // meaningful in thread 0 only
+    if (tid == 0) {
+        for (int st = 0; st < S; ++st) mbar_init(&full_bar[st], 1);
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int pre = min(S, my_count);
+        for (int it = 0; it < pre; ++it) {
+            mbar_arrive_expect_tx(&full_bar[it], in_bytes);
+            bulk_load(stage_in(it), a.x + token_of(it) * H, in_bytes, &full_bar[it]);
+        }
+        loads_issued = pre;
+    }
+
+    int failed_at = -1;
+    for (int it = 0; it < my_count; ++it) {
+        const int st = it % S;
+        const uint32_t parity = (uint32_t)((it / S) & 1);
+        const long long g = token_of(it);
+        int32_t *rows = stage_rows(st);
+
+        // destination rows of this token's K copies (warp 0, lane j = copy j)
+        if (tid < 32) {
+            const int sidx = upper_bound_minus_one(rt.rank_off, rt.R, (int32_t)g);
+            const long long item0 = (long long)rt.rank_off[sidx] * K;
+            int e = -1, row = -1;
+            if (tid < K) {
+                const long long i = g * K + tid;
+                e = __ldg(a.topk_idx + i);
+                const int lr = a.tok2row[i];
+                if (e >= 0 && e < E && lr >= 0) {
+                    const int tile = rt.tile_off[sidx] + (int)((i - item0) / kTileItems);
+                    row = a.scan[(long long)e * rt.ntiles + tile] + lr;
+                    a.row2src[row] = (int32_t)i;
+                } else {
+                    e = -1;
+                }
+                a.tok2row[i] = row;
+                rows[tid] = row;
+            }
+            int dup = 0;   // the same expert twice in one token
+            for (int j = 0; j < K; ++j) {
+                const int ej = __shfl_sync(0xffffffffu, e, j);
+                if (tid < j && e >= 0 && e == ej) dup = 1;
+            }
+            if (__any_sync(0xffffffffu, dup) && tid == 0) set_device_error(a.err, MOE_DEVERR_DUPLICATE);
+        }
+
+        // FP8: the e4m3 row of this stage was last read by the store group of
+        // token it - S; at most S - 1 newer groups may still be reading
+        if (kFp8 && tid == 0 && it >= S) bulk_wait_read_dyn(S - 1);
+        bool ok = mbar_wait_bounded(&full_bar[st], parity);
+        ok = __syncthreads_and(ok);   // also publishes rows[] and orders the buffer reuse above
+        if (!ok) {
+            if (tid == 0) set_device_error(a.err, MOE_DEVERR_COPY_TIMEOUT);
+            failed_at = it;
+            break;
+        }
+
+        if (kFp8) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(stage_in(st));
+            uint2 *q = reinterpret_cast<uint2 *>(stage_q(st));
+            float *sc = stage_sc(st);
+            const int warp = tid >> 5;
+            const int lane = tid & 31;
+            const int nwarps = blockDim.x >> 5;
+            const int hl = lane & 15;
+            for (int b0 = 2 * warp; b0 < nblk; b0 += 2 * nwarps) {   // warp-uniform trip count
+                const int b = b0 + (lane >> 4);
+                const bool valid = b < nblk;
+                const uint4 xin = valid ? src[b * 16 + hl] : make_uint4(0u, 0u, 0u, 0u);
+                uint2 qo;
+                float s;
+                quantize_block16(xin, qo, s);
+                if (valid) {
+                    q[b * 16 + hl] = qo;
+                    if (hl == 0) sc[b] = s;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+        }
+
+        if (tid == 0) {
+            const unsigned char *src = kFp8 ? stage_q(st) : stage_in(st);
+            for (int j = 0; j < K; ++j) {
+                const int row = rows[j];
+                if (row >= 0)
+                    bulk_store(static_cast<unsigned char *>(a.recv_x) + (size_t)row * recv_pitch, src, out_bytes);
+            }
+            bulk_commit();
+            if (kFp8) {
+                // the staged bf16 row has been consumed by the quantise: refill it now
+                if (it + S < my_count) {
+                    mbar_arrive_expect_tx(&full_bar[st], in_bytes);
+                    bulk_load(stage_in(st), a.x + token_of(it + S) * H, in_bytes, &full_bar[st]);
+                    loads_issued = it + S + 1;
+                }
+            } else if (it >= 1 && it - 1 + S < my_count) {
+                // the previous token's store group has read its stage: refill that stage
+                bulk_wait_read<1>();
+                const int pst = (it - 1) % S;
+                mbar_arrive_expect_tx(&full_bar[pst], in_bytes);
+                bulk_load(stage_in(pst), a.x + token_of(it - 1 + S) * H, in_bytes, &full_bar[pst]);
+                loads_issued = it - 1 + S + 1;
+            }
+        }
+        if (kFp8) {
+            const float *sc = stage_sc(st);
+            for (int t = tid; t < K * nblk; t += blockDim.x) {
+                const int j = t / nblk;
+                const int b = t - j * nblk;
+                const int row = rows[j];
+                if (row >= 0) a.recv_scale[(size_t)row * nblk + b] = sc[b];
+            }
+        }
+    }
+
+    if (tid == 0) {
+        if (failed_at >= 0) {
+            // let the loads still in flight land before the block's shared memory goes away
+            for (int t = failed_at; t < loads_issued; ++t)
+                if (!mbar_wait_bounded(&full_bar[t % S], (uint32_t)((t / S) & 1))) break;
+        }
+        bulk_wait_all();
+    }
+}
+
+// --------------------------------------------------------------------------
+// launcher
+// --------------------------------------------------------------------------
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Workspace layout for a worst-case tile count.
+DispatchPlan plan_dispatch(int E, int ntiles) {
+    DispatchPlan p{};
+    p.ntiles = ntiles;
+    const long long n = (long long)E * ntiles;
+    p.nscan_blocks = (int)((n + kScanChunk - 1) / kScanChunk);
+    if (p.nscan_blocks < 1) p.nscan_blocks = 1;
+    p.off_status = kWsHeader;
+    p.off_hist = p.off_status + align256((size_t)p.nscan_blocks * 8);
+    p.off_scan = p.off_hist + align256((size_t)n * 4);
+    p.total = p.off_scan + align256((size_t)(n + 1) * 4);
+    return p;
+}
+
+int max_tiles(int R, int K, long long T) { return (int)((T * K + kTileItems - 1) / kTileItems) + R; }
+
+static int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
+
+int device_sm_count() { return sm_count(); }
+
+cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
+                            bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *offsets,
+                            int32_t *expert_offsets, int32_t *tok2row, int32_t *row2src, void *workspace,
+                            cudaStream_t stream) {
+    const long long T = rt.rank_off[rt.R];
+    const DispatchPlan p = plan_dispatch(E, rt.ntiles);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    int32_t *err = reinterpret_cast<int32_t *>(ws);
+    int32_t *ticket = reinterpret_cast<int32_t *>(ws + 4);
+    unsigned long long *status = reinterpret_cast<unsigned long long *>(ws + p.off_status);
+    int32_t *tile_hist = reinterpret_cast<int32_t *>(ws + p.off_hist);
+    int32_t *scan = reinterpret_cast<int32_t *>(ws + p.off_scan);
+
+    cudaError_t ce = cudaMemsetAsync(ws, 0, p.off_hist, stream);   // error word, ticket, lookback flags
+    if (ce != cudaSuccess) return ce;
+
+    const size_t hist_smem = (size_t)kHistWarps * E * 4;
+    tile_hist_kernel<<<rt.ntiles, kHistThreads, hist_smem, stream>>>(topk_idx, E, K, rt, tile_hist, tok2row, err);
+    if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
+
+    const int n = E * rt.ntiles;
+    lookback_scan_kernel<<<p.nscan_blocks, kScanThreads, 0, stream>>>(tile_hist, scan, n, status, ticket, err);
+    if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
+
+    ScatterArgs a;
+    a.x = static_cast<const __nv_bfloat16 *>(x);
+    a.topk_idx = topk_idx;
+    a.scan = scan;
+    a.recv_x = recv_x;
+    a.recv_scale = recv_scale;
+    a.counts = counts;
+    a.offsets = offsets;
+    a.expert_offsets = expert_offsets;
+    a.tok2row = tok2row;
+    a.row2src = row2src;
+    a.err = err;
+    a.T = (int)T;
+    a.E = E;
+    a.K = K;
+    a.H = H;
+
+    const size_t stage = scatter_stage_bytes(H, K, fp8);
+    const size_t budget = fp8 ? (size_t)100 * 1024 : (size_t)72 * 1024;
+    int stages = (int)(budget / stage);
+    stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+    a.stages = stages;
+    const size_t smem = stage * stages;
+    const int blocks_per_sm = 2;
+    int grid = sm_count() * blocks_per_sm;
+    const int min_grid = (E * rt.R + 1 + 255) / 256;   // enough threads for the offsets pass
+    if (grid > T) grid = (int)T;
+    if (grid < min_grid) grid = min_grid;
+    if (grid < 1) grid = 1;
+    if (fp8) {
+        if ((ce = cudaFuncSetAttribute(scatter_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem)) != cudaSuccess)
+            return ce;
+        scatter_kernel<true><<<grid, 256, smem, stream>>>(a, rt);
+    } else {
+        if ((ce = cudaFuncSetAttribute(scatter_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem)) != cudaSuccess)
+            return ce;
+        scatter_kernel<false><<<grid, 128, smem, stream>>>(a, rt);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

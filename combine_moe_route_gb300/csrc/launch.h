@@ -1,0 +1,36 @@
+// launch.h -- internal declarations shared by the libmoeroute translation
+// units (host-side launchers and the dispatch workspace plan).  Not part of
+// the public ABI, which is include/moe_route.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// Byte offsets inside the dispatch workspace.
+struct DispatchPlan {
+    int ntiles;
+    int nscan_blocks;
+    size_t off_status, off_hist, off_scan, total;
+};
+
+DispatchPlan plan_dispatch(int E, int ntiles);
+int max_tiles(int R, int K, long long T);
+int device_sm_count();
+
+cudaError_t launch_route_topk(const float *logits, int T, int E, int K, int32_t *topk_idx, float *topk_w,
+                              cudaStream_t stream);
+cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
+                            bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *offsets,
+                            int32_t *expert_offsets, int32_t *tok2row, int32_t *row2src, void *workspace,
+                            cudaStream_t stream);
+cudaError_t launch_combine(const void *y, const int32_t *tok2row, const float *topk_w, int T, int K, int H,
+                           bool out_f32, void *out, cudaStream_t stream);
+cudaError_t launch_expert_scale(const void *recv, const float *recv_scale, bool fp8, const int32_t *expert_offsets,
+                                int E, int H, int rows, int identity, void *y, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,234 @@
+/*
+ * moe_route.h -- C ABI of libmoeroute: MoE expert-parallel routing, dispatch
+ * and combine for one GB300 (sm_103a), with R expert-parallel ranks emulated
+ * inside that one GPU's HBM.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [DSD] Perplexity, "Lower latency and higher throughput with multi-node
+ *         DeepSeek deployment": "Expert parallelism", "Quantization",
+ *         "CUDA Graph", "MoE router".
+ *   [EFA] Perplexity, "Enabling trillion-parameter models on AWS EFA":
+ *         "Send and receive buffers", "Dispatch and combine".
+ *   [EPK] lehuy.net, "Decoding high-performance EP kernels" ("Giai ma nhan
+ *         EP hieu suat cao"): "Our task", "Optimising for throughput: ask
+ *         first, send later" > "Dispatch" / "Combine".
+ *
+ * Problem statement ([EPK] "Our task"): R ranks; rank s holds B[s] tokens of
+ * hidden size H; E routed experts, E/R of them on each rank (expert e lives on
+ * rank e / (E/R)); every token is routed to K experts.  Tokens are numbered
+ * globally in rank-major order, g = rank_off[s] + t with
+ * rank_off[s] = B[0] + ... + B[s-1] and T = rank_off[R].
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device (global) memory on the current
+ *     device; pointers marked "host" are ordinary host memory read during the
+ *     call.  The caller allocates and owns every buffer; the library never
+ *     allocates, frees or synchronises (except moe_get_device_error, which
+ *     says so).  Work is enqueued on `stream` and runs asynchronously; the
+ *     calls take no host-device synchronisation, so a sequence of them can be
+ *     captured in a CUDA graph ([DSD] "CUDA Graph").
+ *   - Arrays are dense, row-major, with no padding between rows.
+ *   - Arguments are validated on the host before anything is enqueued; a bad
+ *     argument returns MOE_ERR_INVALID_ARG (or MOE_ERR_UNSUPPORTED for a
+ *     pointer alignment the kernels cannot use) and enqueues nothing.  A CUDA
+ *     launch failure returns MOE_ERR_CUDA.  Errors that only the device can
+ *     see (an expert id out of range, a repeated expert within one token, a
+ *     bounded device wait that ran out) are recorded in the workspace's error
+ *     word and read with moe_get_device_error.  No call aborts, traps or
+ *     throws across this boundary.
+ *   - bf16 is IEEE binary32 truncated to its top 16 bits with round to
+ *     nearest even; fp8 is OCP E4M3 (bias 7, largest finite 448, no inf).
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ROUTE_ABI_VERSION 1
+
+/* Symbols of this header are the only ones the shared library exports. */
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* Limits checked by the argument validation. */
+#define MOE_MAX_RANKS 256      /* R */
+#define MOE_MAX_EXPERTS 1024   /* E */
+#define MOE_MAX_TOPK 32        /* K */
+#define MOE_MAX_HIDDEN 16384   /* H */
+
+/* A CUDA stream (the same type as cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* a NULL, a size out of range, an inconsistent shape */
+    MOE_ERR_UNSUPPORTED = 2,   /* a pointer not aligned to 16 bytes */
+    MOE_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    MOE_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
+    MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (see moe_get_device_error) */
+    MOE_ERR_BAD_ROUTING = 6    /* device: expert id out of range or repeated within a token */
+} moe_status;
+
+typedef enum {
+    MOE_DTYPE_BF16 = 0,
+    MOE_DTYPE_FP8_E4M3 = 1,
+    MOE_DTYPE_FP32 = 2
+} moe_dtype;
+
+/* Device error word bits (moe_get_device_error's *host_code). */
+#define MOE_DEVERR_EXPERT_RANGE 0x1   /* a topk_idx entry outside [0, E) */
+#define MOE_DEVERR_DUPLICATE 0x2      /* the same expert twice in one token's top-K */
+#define MOE_DEVERR_SCAN_TIMEOUT 0x4   /* the decoupled-lookback wait ran out */
+#define MOE_DEVERR_COPY_TIMEOUT 0x8   /* a bulk-copy barrier wait ran out */
+
+/* Returns MOE_ROUTE_ABI_VERSION of the loaded library. */
+MOE_API int moe_abi_version(void);
+
+/* A static, NUL-terminated English description of a moe_status value. */
+MOE_API const char *moe_strerror(int status);
+
+/*
+ * moe_route_topk -- the router's top-K ([DSD] "MoE router": a sort that keeps
+ * the indices of the selected scores; "Expert parallelism": each token goes to
+ * K of the routed experts and their outputs are summed with weights).
+ *
+ *   logits   device, fp32 [T, E]     router scores.  NaN is not supported.
+ *   T        number of tokens, >= 0 (T == 0 enqueues nothing).
+ *   E        experts, 1..MOE_MAX_EXPERTS.
+ *   K        experts per token, 1..min(E, MOE_MAX_TOPK).
+ *   topk_idx device, int32 [T, K]    out: the K largest logits' expert ids, by
+ *            descending logit; equal logits go to the smaller id (+0 and -0
+ *            count as equal).
+ *   topk_w   device, fp32 [T, K]     out: softmax over the K selected logits,
+ *            w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), summed in j order.
+ * Errors: MOE_ERR_INVALID_ARG for T < 0, E or K out of range, NULL pointers
+ * with T > 0; MOE_ERR_CUDA if the launch fails.
+ */
+MOE_API moe_status moe_route_topk(const float *logits, int T, int E, int K,
+                          int32_t *topk_idx, float *topk_w, moe_stream_t stream);
+
+/*
+ * Bytes of device workspace moe_dispatch needs for these sizes (an upper bound
+ * that depends only on R, E, K and T = sum B).  Returns 0 for sizes that
+ * moe_dispatch would reject.
+ */
+MOE_API size_t moe_dispatch_workspace_bytes(int R, int E, int K, int64_t T);
+
+/*
+ * moe_dispatch -- count, exclusive scan and scatter ([EPK] "Optimising for
+ * throughput" > "Dispatch": count the tokens per destination, exchange the
+ * counts, let a prefix sum fix a conflict-free layout, copy each token to its
+ * slot; [EFA] "Dispatch and combine": per-expert counts by shared-memory
+ * atomics, a prefix sum for the offsets, rows packed into the input of the
+ * grouped GEMM).  With every rank in one HBM the count exchange is a read of
+ * the count matrix and the copy is one hop into the destination rank's rows.
+ *
+ *   x          device, bf16 [T, H], 16-byte aligned: the tokens of all ranks,
+ *              rank-major.
+ *   topk_idx   device, int32 [T, K]: the routing (e.g. from moe_route_topk).
+ *   R          ranks, 1..MOE_MAX_RANKS; E % R == 0.
+ *   B          HOST, int32 [R]: tokens per rank, each >= 0; T = sum B and
+ *              T * K < 2^31.
+ *   E, K       as for moe_route_topk (K <= MOE_MAX_TOPK).
+ *   H          hidden size, 8..MOE_MAX_HIDDEN, a multiple of 8; a multiple of
+ *              128 when recv_dtype is MOE_DTYPE_FP8_E4M3.
+ *   recv_dtype MOE_DTYPE_BF16 (copy) or MOE_DTYPE_FP8_E4M3 (quantise once per
+ *              token: per 128-channel block, amax = max |x| floored at 2^-64,
+ *              scale = amax / 448 and inv = 448 / amax (IEEE fp32 divisions),
+ *              q = e4m3(x * inv) with round-to-nearest-even and saturation to
+ *              +-448; [DSD] "Quantization").
+ *   recv_x     device [T*K, H] of recv_dtype, 16-byte aligned: out.  Rows are
+ *              grouped by expert (expert_offsets), within an expert by source
+ *              rank (offsets), within a rank by ascending token; rank r's
+ *              receive window is rows [expert_offsets[r*E/R],
+ *              expert_offsets[(r+1)*E/R]).
+ *   recv_scale device fp32 [T*K, H/128], 16-byte aligned: out, FP8 only
+ *              (ignored and may be NULL for bf16).  Dequantised value =
+ *              e4m3 value * recv_scale[row, h/128].
+ *   counts     device int32 [E*R]: out, counts[e*R + s] = tokens of rank s
+ *              routed to expert e.
+ *   offsets    device int32 [E*R + 1]: out, exclusive prefix sum of counts in
+ *              (e, s) order; offsets[E*R] = T*K.
+ *   expert_offsets device int32 [E + 1]: out, offsets[e*R].
+ *   tok2row    device int32 [T*K]: out, the row holding copy j of token g is
+ *              tok2row[g*K + j] (combine's gather map).
+ *   row2src    device int32 [T*K]: out, row2src[row] = g*K + j (the inverse).
+ *   workspace  device, >= moe_dispatch_workspace_bytes(R, E, K, T) bytes,
+ *              16-byte aligned; its first 4 bytes are the device error word.
+ *              Calls that share a workspace must not overlap in time.
+ * Errors: MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE as
+ * above, MOE_ERR_CUDA on a launch failure.  T == 0 writes zeros to counts,
+ * offsets and expert_offsets and launches no kernel.  Bad routing is reported
+ * through the error word; the outputs are then unspecified, but no write
+ * leaves the buffers above.
+ */
+MOE_API moe_status moe_dispatch(const void *x, const int32_t *topk_idx,
+                        int R, const int32_t *B, int E, int K, int H,
+                        moe_dtype recv_dtype, void *recv_x, float *recv_scale,
+                        int32_t *counts, int32_t *offsets, int32_t *expert_offsets,
+                        int32_t *tok2row, int32_t *row2src,
+                        void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_expert_scale -- stand-in for the grouped expert GEMM (which is not part
+ * of this library): y[row] = bf16(xhat * s_e) with s_e = 1 + e/256 for the
+ * expert e whose rows [expert_offsets[e], expert_offsets[e+1]) hold `row`
+ * (s_e = 1 when identity != 0); xhat is the bf16 value, or for an FP8 buffer
+ * e4m3 value * recv_scale (one fp32 multiply).
+ *
+ *   recv_x, recv_scale, recv_dtype   as produced by moe_dispatch.
+ *   expert_offsets device int32 [E + 1]; rows = expert_offsets[E] = T*K.
+ *   y          device bf16 [rows, H], 16-byte aligned: out.
+ * Errors: MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_CUDA.
+ */
+MOE_API moe_status moe_expert_scale(const void *recv_x, const float *recv_scale, moe_dtype recv_dtype,
+                            const int32_t *expert_offsets, int E, int H, int rows,
+                            int identity, void *y, moe_stream_t stream);
+
+/*
+ * moe_combine -- gather each token's K expert outputs and take their
+ * routing-weighted sum ([EPK] "Optimising for throughput" > "Combine": undo
+ * the dispatch permutation and add up each token's contributions with the
+ * routing dispatch produced; [EFA] "Dispatch and combine": the receiver
+ * accumulates the returned tokens into the output).
+ *
+ *   y          device bf16 [T*K, H], 16-byte aligned: expert outputs in the
+ *              dispatch row order.
+ *   tok2row    device int32 [T*K]: from moe_dispatch.  Entries outside
+ *              [0, T*K) contribute nothing.
+ *   topk_w     device fp32 [T, K]: routing weights.
+ *   out_dtype  MOE_DTYPE_BF16 or MOE_DTYPE_FP32.
+ *   out        device [T, H] of out_dtype, 16-byte aligned:
+ *              out[g] = sum_{j=0..K-1} topk_w[g,j] * y[tok2row[g*K+j]],
+ *              accumulated in fp32 by fused multiply-add in the fixed order
+ *              j = 0, 1, ..., K-1 from +0, then rounded to bf16 (nearest even)
+ *              or stored as fp32.
+ * Errors: MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_CUDA.
+ */
+MOE_API moe_status moe_combine(const void *y, const int32_t *tok2row, const float *topk_w,
+                       int T, int K, int H, moe_dtype out_dtype, void *out,
+                       moe_stream_t stream);
+
+/*
+ * moe_get_device_error -- SYNCHRONOUS: waits for `stream`, then copies the
+ * dispatch workspace's error word (an OR of MOE_DEVERR_* bits, 0 if none) to
+ * *host_code.  Returns MOE_ERR_TIMEOUT if a timeout bit is set, else
+ * MOE_ERR_BAD_ROUTING if a routing bit is set, else MOE_OK (MOE_ERR_CUDA if
+ * the copy fails, MOE_ERR_INVALID_ARG for NULL pointers).  The word is reset
+ * by the next moe_dispatch on that workspace.
+ */
+MOE_API moe_status moe_get_device_error(const void *workspace, int32_t *host_code, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_H */

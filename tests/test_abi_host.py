@@ -1,0 +1,156 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+public header declares, and its host-side validation rejects bad arguments
+before anything reaches CUDA.
+
+Every call below either fails validation or has nothing to do (T == 0), so
+none of them touches device memory; the fake pointers are never used.  Keep
+it that way: a call that passed validation with a fake pointer would launch a
+kernel on a machine that has a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+OK, INVALID, UNSUPPORTED, CUDA, WORKSPACE = 0, 1, 2, 3, 4
+BF16, FP8, FP32 = 0, 1, 2
+FAKE = 0x100000          # a 16-byte aligned non-NULL address; never dereferenced by a rejected call
+FAKE_MISALIGNED = 0x100008
+
+
+def _declared_functions():
+    names = []
+    for f in sorted(os.listdir(HEADER_DIR)):
+        if f.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, f)).read()
+            names += re.findall(r"^MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from combine_moe_route_gb300 import build, binding
+    build.build()
+    return binding.load_library()
+
+
+def test_header_declares_the_abi():
+    names = set(_declared_functions())
+    assert {"moe_route_topk", "moe_dispatch", "moe_combine", "moe_dispatch_workspace_bytes",
+            "moe_expert_scale", "moe_get_device_error", "moe_strerror", "moe_abi_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_library_exports_nothing_else(lib):
+    import subprocess
+    from combine_moe_route_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.library_path()], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("nm not available")
+    exported = {line.split()[-1] for line in out.stdout.splitlines() if line.strip()}
+    assert exported == set(_declared_functions())
+
+
+def test_version_and_strerror(lib):
+    assert lib.moe_abi_version() == 1
+    for s in range(7):
+        assert len(lib.moe_strerror(s)) > 5
+    assert b"unknown" in lib.moe_strerror(99)
+
+
+def test_route_validation(lib):
+    f = lib.moe_route_topk
+    assert f(FAKE, -1, 16, 2, FAKE, FAKE, None) == INVALID
+    assert f(FAKE, 4, 16, 0, FAKE, FAKE, None) == INVALID
+    assert f(FAKE, 4, 16, 17, FAKE, FAKE, None) == INVALID
+    assert f(FAKE, 4, 1025, 2, FAKE, FAKE, None) == INVALID
+    assert f(FAKE, 4, 64, 33, FAKE, FAKE, None) == INVALID
+    assert f(None, 4, 16, 2, FAKE, FAKE, None) == INVALID
+    assert f(None, 0, 16, 2, None, None, None) == OK        # empty: nothing enqueued
+
+
+def _B(*v):
+    return np.array(v, dtype=np.int32)
+
+
+def _dispatch(lib, B, E=16, K=2, H=256, dtype=BF16, x=FAKE, recv=FAKE, scale=FAKE, ws=FAKE, ws_bytes=1 << 30,
+              idx=FAKE):
+    return lib.moe_dispatch(x, idx, B.size, B.ctypes.data, E, K, H, dtype, recv, scale, FAKE, FAKE, FAKE,
+                            FAKE, FAKE, ws, ws_bytes, None)
+
+
+def test_dispatch_validation(lib):
+    B = _B(3, 0, 5, 1)
+    assert lib.moe_dispatch(FAKE, FAKE, 0, B.ctypes.data, 16, 2, 256, BF16, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                            FAKE, FAKE, 1 << 30, None) == INVALID                       # R = 0
+    assert _dispatch(lib, _B(*([1] * 257)), E=257) == INVALID                         # R > 256
+    assert _dispatch(lib, B, E=18) == INVALID                                         # E % R
+    assert _dispatch(lib, B, H=12) == INVALID                                         # H % 8
+    assert _dispatch(lib, B, H=16392) == INVALID                                      # H too large
+    assert _dispatch(lib, B, H=264, dtype=FP8) == INVALID                             # FP8 needs H % 128
+    assert _dispatch(lib, B, dtype=FP32) == INVALID                                   # no fp32 payload
+    assert _dispatch(lib, _B(3, -1, 5, 1)) == INVALID                                 # negative B
+    assert _dispatch(lib, _B(1 << 30, 1 << 30, 0, 0)) == INVALID                      # T*K overflows int32
+    assert _dispatch(lib, B, K=17) == INVALID                                         # K > E
+    assert _dispatch(lib, B, x=None) == INVALID
+    assert _dispatch(lib, B, dtype=FP8, scale=None) == INVALID
+    assert _dispatch(lib, B, ws=None) == WORKSPACE
+    need = lib.moe_dispatch_workspace_bytes(4, 16, 2, 9)
+    assert need > 256
+    assert _dispatch(lib, B, ws_bytes=256) == WORKSPACE                                # header only
+    assert _dispatch(lib, B, x=FAKE_MISALIGNED, ws_bytes=need) == UNSUPPORTED
+    assert _dispatch(lib, B, recv=FAKE_MISALIGNED) == UNSUPPORTED
+    assert _dispatch(lib, B, ws=FAKE_MISALIGNED) == UNSUPPORTED
+    assert _dispatch(lib, B, dtype=FP8, scale=FAKE_MISALIGNED) == UNSUPPORTED
+
+
+def test_workspace_bytes(lib):
+    f = lib.moe_dispatch_workspace_bytes
+    assert f(0, 16, 2, 10) == 0 and f(4, 18, 2, 10) == 0 and f(4, 16, 0, 10) == 0 and f(4, 16, 2, -1) == 0
+    assert f(4, 16, 2, 1 << 30) == 0
+    sizes = [f(8, 256, 8, T) for T in (0, 1, 1000, 32768)]
+    assert all(a <= b for a, b in zip(sizes, sizes[1:])) and sizes[0] > 0
+    assert f(8, 256, 8, 32768) < 8 << 20        # small next to the payload
+
+
+def test_combine_and_expert_validation(lib):
+    c = lib.moe_combine
+    assert c(FAKE, FAKE, FAKE, -1, 2, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE, FAKE, FAKE, 4, 0, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE, FAKE, FAKE, 4, 33, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE, FAKE, FAKE, 4, 2, 250, BF16, FAKE, None) == INVALID
+    assert c(FAKE, FAKE, FAKE, 4, 2, 256, FP8, FAKE, None) == INVALID
+    assert c(None, FAKE, FAKE, 4, 2, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE_MISALIGNED, FAKE, FAKE, 4, 2, 256, BF16, FAKE, None) == UNSUPPORTED
+    assert c(FAKE, FAKE, FAKE, 4, 2, 256, FP32, FAKE_MISALIGNED, None) == UNSUPPORTED
+    assert c(None, None, None, 0, 2, 256, BF16, None, None) == OK
+    e = lib.moe_expert_scale
+    assert e(FAKE, FAKE, BF16, FAKE, 0, 256, 8, 0, FAKE, None) == INVALID
+    assert e(FAKE, FAKE, FP8, FAKE, 4, 200, 8, 0, FAKE, None) == INVALID
+    assert e(FAKE, None, FP8, FAKE, 4, 256, 8, 0, FAKE, None) == INVALID
+    assert e(FAKE_MISALIGNED, FAKE, BF16, FAKE, 4, 256, 8, 0, FAKE, None) == UNSUPPORTED
+    assert e(None, None, BF16, None, 4, 256, 0, 0, None, None) == OK
+
+
+def test_get_device_error_validation(lib):
+    code = ctypes.c_int32(0)
+    assert lib.moe_get_device_error(None, ctypes.byref(code), None) == INVALID
+    assert lib.moe_get_device_error(FAKE, None, None) == INVALID
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    from combine_moe_route_gb300 import binding
+    with pytest.raises(ValueError):
+        binding.route_topk(torch.zeros(4, 16), 2)
+    with pytest.raises(ValueError):
+        binding.combine(torch.zeros(8, 16, dtype=torch.bfloat16), torch.zeros(8, dtype=torch.int32),
+                        torch.zeros(4, 2))
