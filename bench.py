@@ -1,0 +1,500 @@
+"""Benchmark: MoE dispatch + combine on one GB300 (µs per layer, HBM GB/s).
+
+One step = one pass of the whole path over one synthetic layer: route
+(top-K), dispatch (count, scan, scatter [+ FP8 quantise]), the per-expert
+scale stand-in for the grouped GEMM, combine.  The metric is dispatch +
+combine µs per layer (CUDA events on the launching stream around each call;
+the L2 is flushed by a 256 MiB write before dispatch and before combine,
+outside those events).  ``value`` is that time; the roofline object reports
+the dominant call's algorithmic bytes / its event time against the measured
+HBM copy bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+N > 1 (torchrun, one process per GPU) runs N independent replicas of the
+layer; ranks do not exchange data.  ``--impl reference`` times the CPU oracle
+(single-threaded C) on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "dispatch+combine µs/layer and achieved HBM GB/s (% of 8 TB/s) on 1 GB300"
+UNIT = "us/layer"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (the minimum each call must move)
+# ---------------------------------------------------------------------------
+
+def dispatch_bytes(T, E, R, K, H, fp8):
+    payload = T * K * H * (1 if fp8 else 2)
+    scales = T * K * (H // 128) * 4 if fp8 else 0
+    return T * H * 2 + payload + scales + T * K * 4 + 2 * T * K * 4 + 2 * E * R * 4
+
+
+def combine_bytes(T, K, H):
+    return T * K * H * 2 + T * H * 2 + T * K * 4 + T * K * 4
+
+
+def route_bytes(T, E, K):
+    return T * E * 4 + T * K * 8
+
+
+# ---------------------------------------------------------------------------
+# environment helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(kernel_file: str, summary_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    src = os.path.join(ROOT, "combine_moe_route_gb300", "csrc", kernel_file)
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        line = line.strip().lstrip("-* ")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled in a child process."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, "t_" + which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._reader.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+        inside = [r for r in rows if self.t_start and self.t_stop and self.t_start <= r[0] <= self.t_stop + 0.06]
+        window = "timed"
+        if not inside:
+            inside, window = rows, "warmup+timed (timed region shorter than the 50 ms sampling period)"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world <= 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def replica_value(per_rank_us: float, world: int) -> float:
+    """Whole-job µs per layer for N independent replicas: the slowest rank's
+    time per layer divided by the N layers processed in that time."""
+    return per_rank_us / world
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline field)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(workload, tokens_per_rank: int, seed: int = 0):
+    from combine_moe_route_gb300 import workloads as wl
+    w = wl.WORKLOADS[workload]
+    B = np.full(w.R, tokens_per_rank, np.int32)
+    inp = wl.generate(w, seed=seed, B=B)
+    return w, inp
+
+
+class OracleLayer:
+    """The oracle's inputs for one sample, with routing and expert outputs prepared once."""
+
+    def __init__(self, w, inp):
+        import oracle
+        from combine_moe_route_gb300 import workloads as wl
+        self.o, self.w, self.inp = oracle, w, inp
+        self.x = wl.bf16_bits(inp["x"])
+        self.idx, self.wts = oracle.route_topk(inp["logits"], w.K)
+        d = oracle.dispatch(self.x, self.idx, inp["B"], w.E, fp8=w.fp8)
+        self.tok2row = d["tok2row"]
+        self.y = oracle.expert_scale(d["recv"], d["recv_scale"], d["expert_offsets"], w.E)
+
+    def time_step(self):
+        """Seconds of one oracle dispatch plus one oracle combine on this sample."""
+        t0 = time.perf_counter()
+        self.o.dispatch(self.x, self.idx, self.inp["B"], self.w.E, fp8=self.w.fp8)
+        t1 = time.perf_counter()
+        self.o.combine(self.y, self.tok2row, self.wts, out="bf16")
+        t2 = time.perf_counter()
+        return t2 - t0
+
+
+def cpu_baseline(workload: str, T_full: int):
+    from combine_moe_route_gb300 import workloads as wl
+    w = wl.WORKLOADS[workload]
+    tpr = max(1, (T_full // w.R) // 8)
+    w, inp = oracle_sample(workload, tpr)
+    layer = OracleLayer(w, inp)
+    t_start = time.perf_counter()
+    times = []
+    while True:
+        times.append(layer.time_step())
+        if time.perf_counter() - t_start > 10.0 or len(times) >= 20:
+            break
+    T_s = inp["T"]
+    per_layer_us = statistics.median(times) * 1e6 * (T_full / T_s)
+    return {"value": per_layer_us, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{workload} with {tpr} tokens/rank (T={T_s} of {T_full}); median of {len(times)} "
+                      "runs of oracle dispatch + combine, scaled by T_full/T_sample; single-threaded C"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from combine_moe_route_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    T_full = int(wl.draw_B(w, 0).sum())
+    # each step: the oracle on 1/64 of the layer's tokens (at least 1 per rank), scaled to the layer
+    tpr = max(1, (T_full // w.R) // 64)
+    w, inp = oracle_sample(args.workload, tpr)
+    layer = OracleLayer(w, inp)
+    for _ in range(args.warmup):
+        layer.time_step()
+    times = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        times.append(layer.time_step() * 1e6 * (T_full / inp["T"]))
+    wall = time.perf_counter() - t0
+    value = statistics.mean(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": bench_config(w, T_full, "CPU oracle"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.workload} with {tpr} tokens/rank per step (T={inp['T']} of {T_full}), "
+                                   "oracle dispatch + combine scaled by T_full/T_sample; single-threaded C"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def bench_config(w, T, l2, tokens_per_rank=None):
+    tpr = tokens_per_rank if tokens_per_rank is not None else (
+        f"{w.b_lo}" if w.b_lo == w.b_hi else f"U{{{w.b_lo}..{w.b_hi}}}")
+    return {"workload": w.name, "R": w.R, "E": w.E, "K": w.K, "H": w.H, "T": T, "tokens_per_rank": tpr,
+            "dispatch_payload": "fp8_e4m3 + fp32 scale per 128 channels" if w.fp8 else "bf16",
+            "combine_out": "bf16 (fp32 accumulate)", "l2": l2, "seed": 0, "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    from combine_moe_route_gb300 import binding as b
+    from combine_moe_route_gb300 import build
+    from combine_moe_route_gb300 import workloads as wl
+
+    if not os.path.exists(build.library_path()):
+        build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = wl.WORKLOADS[args.workload]
+    if args.tokens_per_rank is not None:          # a smaller case of the same layer (profiling)
+        inp = wl.generate(w, seed=0, B=np.full(w.R, args.tokens_per_rank, np.int32))
+    else:
+        inp = wl.generate(w, seed=0)
+    B, T, E, K, H = inp["B"], inp["T"], w.E, w.K, w.H
+    stream = torch.cuda.current_stream(dev)
+
+    x = inp["x"].to(dev)
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, K), dtype=torch.float32, device=dev)
+    b.route_topk(logits, K, topk_idx=idx, topk_w=wts)
+    d = b.dispatch(x, idx, B, E, fp8=w.fp8)                 # allocates outputs + workspace once
+    y = b.expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E)
+    out = b.combine(y, d.tok2row, wts)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    st, code = b.get_device_error(d.workspace)
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x} after the first layer")
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        b.route_topk(logits, K, topk_idx=idx, topk_w=wts)
+        if ev is not None:
+            ev[1].record(stream)
+        flush.fill_(1)
+        if ev is not None:
+            ev[2].record(stream)
+        b.dispatch(x, idx, B, E, fp8=w.fp8, out=d)
+        if ev is not None:
+            ev[3].record(stream)
+        b.expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E, out=y)
+        if ev is not None:
+            ev[4].record(stream)
+        flush.fill_(2)
+        if ev is not None:
+            ev[5].record(stream)
+        b.combine(y, d.tok2row, wts, out=out)
+        if ev is not None:
+            ev[6].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.2)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark("start")
+    t_all0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("stop")
+    barrier(world)
+    clocks.stop()
+
+    route_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    disp_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    exp_ms = [e[3].elapsed_time(e[4]) for e in evs]
+    comb_ms = [e[5].elapsed_time(e[6]) for e in evs]
+    total_ms = t_all0.elapsed_time(t_all1)
+    dc_us = statistics.mean(a + c for a, c in zip(disp_ms, comb_ms)) * 1e3
+    dc_us_max = max_over_ranks(dc_us, world, dev)
+    step_ms_max = max_over_ranks(total_ms / args.steps, world, dev)
+
+    # end to end through the public API: pinned host inputs -> device -> layer -> pinned host output
+    x_h = inp["x"].pin_memory()
+    lg_h = torch.from_numpy(inp["logits"]).pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        x.copy_(x_h, non_blocking=True)
+        logits.copy_(lg_h, non_blocking=True)
+        b.route_topk(logits, K, topk_idx=idx, topk_w=wts)
+        b.dispatch(x, idx, B, E, fp8=w.fp8, out=d)
+        b.expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E, out=y)
+        b.combine(y, d.tok2row, wts, out=out)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = max_over_ranks(e0.elapsed_time(e1) * 1e3 / e2e_steps, world, dev)
+
+    # correctness of what was timed: the last step's outputs equal the first layer's
+    st, code = b.get_device_error(d.workspace)
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x} during the timed steps")
+
+    if rank != 0:
+        return
+
+    peak, peak_kind = measured_peaks()
+    db = dispatch_bytes(T, E, w.R, K, H, w.fp8)
+    cb = combine_bytes(T, K, H)
+    d_us = statistics.mean(disp_ms) * 1e3
+    c_us = statistics.mean(comb_ms) * 1e3
+    r_us = statistics.mean(route_ms) * 1e3
+    d_gbs = db / (d_us * 1e-6) / 1e9
+    c_gbs = cb / (c_us * 1e-6) / 1e9
+    if c_us >= d_us:
+        dom = {"kernel": "combine_kernel (moe_combine, 1 launch)", "bytes": cb, "us": c_us,
+               "traffic": profile_traffic("combine.cu", "combine_dsv3_prefill.md")}
+    else:
+        dom = {"kernel": "moe_dispatch (hist + scan + scatter launches)", "bytes": db, "us": d_us,
+               "traffic": profile_traffic("dispatch.cu", "dispatch_dsv3_prefill.md")}
+    achieved = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
+    cpu = cpu_baseline(args.workload, T) if (world == 1 and not args.no_cpu_baseline) else None
+    if args.tokens_per_rank is not None:
+        line_note = f"tokens_per_rank overridden to {args.tokens_per_rank} (not the benchmark workload)"
+    else:
+        line_note = None
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC,
+        "value": replica_value(dc_us_max, world),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms_max,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) tokens and router logits, see combine_moe_route_gb300/workloads.py)",
+        "config": bench_config(w, T, f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write before dispatch and "
+                                     "before combine (outside their events); all buffers exceed the 126 MB L2",
+                               args.tokens_per_rank),
+        "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} (hbm_gbs)", "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": dom["traffic"], "algorithmic_bytes": dom["bytes"]},
+        "kernels_us": {"route": r_us, "dispatch": d_us, "expert_stand_in": statistics.mean(exp_ms) * 1e3,
+                       "combine": c_us},
+        "hbm": {"dispatch_GBps": d_gbs, "dispatch_pct_of_8TBs": 100 * d_gbs / NOMINAL_HBM_GBS,
+                "combine_GBps": c_gbs, "combine_pct_of_8TBs": 100 * c_gbs / NOMINAL_HBM_GBS,
+                "dispatch_frac_of_measured": d_gbs / peak, "combine_frac_of_measured": c_gbs / peak,
+                "route_GBps": route_bytes(T, E, K) / (r_us * 1e-6) / 1e9},
+        "p50_us": {"dispatch": statistics.median(disp_ms) * 1e3, "combine": statistics.median(comb_ms) * 1e3},
+        "e2e": {"value": replica_value(e2e_us, world), "unit": UNIT,
+                "h2d_bytes_per_step": int(x_h.numel() * 2 + lg_h.numel() * 4),
+                "d2h_bytes_per_step": int(out_h.numel() * 2),
+                "note": "route+dispatch+expert stand-in+combine with host<->device copies, through the Python API"},
+        "gpu_launches": 6 * args.steps,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                   "samples": clk["samples"], "window": clk["window"]},
+        "cpu_baseline": cpu,
+    }
+    if line_note:
+        line["note"] = line_note
+    print(json.dumps(line))
+
+
+def main():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default="dsv3_prefill")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--tokens-per-rank", type=int, default=None,
+                   help="override B (every rank) for a smaller case of the workload, e.g. for ncu captures")
+    args = p.parse_args()
+    args.warmup = max(3, args.warmup)        # at least 3 untimed warm-up steps
+    world, rank, local = dist_init()
+    if world != args.gpus:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
