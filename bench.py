@@ -424,7 +424,7 @@ def run_ours(args, world, rank, local):
                "traffic": profile_traffic("combine.cu", "combine_dsv3_prefill.md")}
     else:
         dom = {"kernel": "moe_dispatch (hist + scan + scatter launches)", "bytes": db, "us": d_us,
-               "traffic": profile_traffic("dispatch.cu", "dispatch_dsv3_prefill.md")}
+               "traffic": profile_traffic("dispatch.cu", "scatter_dsv3_prefill.md")}
     achieved = dom["bytes"] / (dom["us"] * 1e-6) / 1e9
     cpu = cpu_baseline(args.workload, T) if (world == 1 and not args.no_cpu_baseline) else None
     if args.tokens_per_rank is not None:
