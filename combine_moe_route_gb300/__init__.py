@@ -13,7 +13,7 @@ from importlib import import_module
 _API = {
     "route_topk", "dispatch", "combine", "expert_scale", "dispatch_workspace_bytes",
     "get_device_error", "abi_version", "strerror", "MoeError", "DispatchResult",
-    "moe_layer", "library_path", "load_library", "MOE_OK",
+    "moe_layer", "library_path", "load_library", "MOE_OK", "dispatch_noalloc",
 }
 
 __all__ = sorted(_API) + ["workloads"]

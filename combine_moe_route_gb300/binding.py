@@ -279,3 +279,42 @@ def moe_layer(x: torch.Tensor, logits: torch.Tensor, B, E: int, K: int, *, fp8: 
     y = expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E, identity=identity, stream=stream)
     o = combine(y, d.tok2row, w, out_dtype=out_dtype, stream=stream)
     return dict(topk_idx=idx, topk_w=w, dispatch=d, y=y, out=o)
+
+
+# ---------------------------------------------------------------------------
+# dispatch without a caller-supplied workspace
+# ---------------------------------------------------------------------------
+
+def dispatch_noalloc(x: torch.Tensor, topk_idx: torch.Tensor, B, E: int, *, fp8: bool = False,
+                     out: DispatchResult, stream=None) -> DispatchResult:
+    """moe_dispatch_noalloc: like ``dispatch`` but with the library's static
+    device scratch as workspace, for callers that cannot allocate device memory.
+    Every output buffer must be passed in ``out`` (its ``workspace`` is ignored);
+    nothing is allocated here.  The first call on a device must come before any
+    stream capture; calls that overlap on the GPU race on the shared scratch."""
+    lib = load_library()
+    fn = lib.moe_dispatch_noalloc
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    fn.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    fn.restype = i32
+    _dev(x, "x", torch.bfloat16)
+    T, H = x.shape
+    _dev(topk_idx, "topk_idx", torch.int32)
+    K = topk_idx.shape[1]
+    Bh = _host_B(B)
+    R = Bh.size
+    if int(Bh.astype(np.int64).sum()) != T:
+        raise ValueError(f"sum(B) = {int(Bh.sum())} does not match x.shape[0] = {T}")
+    rows = T * K
+    _dev(out.recv_x, "recv_x", (torch.float8_e4m3fn, torch.uint8) if fp8 else torch.bfloat16, (rows, H))
+    if fp8:
+        _dev(out.recv_scale, "recv_scale", torch.float32, (rows, H // 128))
+    for name, n in (("counts", E * R), ("offsets", E * R + 1), ("expert_offsets", E + 1),
+                    ("tok2row", rows), ("row2src", rows)):
+        _dev(getattr(out, name), name, torch.int32, (n,))
+    with torch.cuda.device(x.device):
+        _check(fn(_ptr(x), _ptr(topk_idx), R, Bh.ctypes.data, E, K, H, _DTYPE_FP8 if fp8 else _DTYPE_BF16,
+                  _ptr(out.recv_x), _ptr(out.recv_scale) if fp8 else None, _ptr(out.counts), _ptr(out.offsets),
+                  _ptr(out.expert_offsets), _ptr(out.tok2row), _ptr(out.row2src),
+                  _stream_handle(stream, x.device)), "moe_dispatch_noalloc")
+    return out

@@ -178,6 +178,43 @@ MOE_API moe_status moe_dispatch(const void *x, const int32_t *topk_idx,
                         void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * moe_dispatch_noalloc -- moe_dispatch without a caller-supplied workspace,
+ * for callers that cannot allocate device memory: a plugin whose memory is
+ * owned by a host framework, a serving loop that must not allocate on its hot
+ * path, or code recording a CUDA graph (where cudaMalloc is not permitted).
+ * The pages this library follows have no counterpart to it.
+ *
+ * Arguments and outputs are those of moe_dispatch, minus the workspace.  The
+ * workspace is a device array of MOE_NOALLOC_SCRATCH_BYTES bytes that the
+ * library holds on every GPU that loads it, for the life of the process.
+ * Neither this call nor its set-up calls cudaMalloc, cudaFree or any other
+ * allocating routine.
+ *   - Set-up: the first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress, with the device current) and keeps it for the
+ *     life of the process (a cudaDeviceReset invalidates it).  Make that first
+ *     call on each device before any stream capture.
+ *   - Size limit: a call for which moe_dispatch_workspace_bytes(R, E, K, T)
+ *     exceeds MOE_NOALLOC_SCRATCH_BYTES returns MOE_ERR_WORKSPACE and enqueues
+ *     nothing (1 MiB covers, for example, E = 256 experts with T*K up to
+ *     about 880 000 routed copies).
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     last call's contents; each call clears the parts that must start at
+ *     zero.  Calls that overlap on the GPU (other streams, other threads)
+ *     race on it and must be ordered by the caller.
+ *   - Device-side routing errors are recorded in the array's error word, which
+ *     the caller cannot read; check the routing with moe_dispatch and
+ *     moe_get_device_error where that matters.
+ * Other errors: as moe_dispatch.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+MOE_API moe_status moe_dispatch_noalloc(const void *x, const int32_t *topk_idx,
+                                        int R, const int32_t *B, int E, int K, int H,
+                                        moe_dtype recv_dtype, void *recv_x, float *recv_scale,
+                                        int32_t *counts, int32_t *offsets, int32_t *expert_offsets,
+                                        int32_t *tok2row, int32_t *row2src, moe_stream_t stream);
+
+/*
  * moe_expert_scale -- stand-in for the grouped expert GEMM (which is not part
  * of this library): y[row] = bf16(xhat * s_e) with s_e = 1 + e/256 for the
  * expert e whose rows [expert_offsets[e], expert_offsets[e+1]) hold `row`
