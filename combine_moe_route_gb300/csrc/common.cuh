@@ -19,9 +19,9 @@ constexpr int kTileItems = kHistThreads * kItemsPerThread;   // 2048
 constexpr int kItemsPerWarp = kTileItems / kHistWarps;       // 256
 
 // Decoupled-lookback scan: elements per block.
-constexpr int kScanThreads = 256;
+constexpr int kScanThreads = 1024;
 constexpr int kScanPerThread = 8;
-constexpr int kScanChunk = kScanThreads * kScanPerThread;   // 2048
+constexpr int kScanChunk = kScanThreads * kScanPerThread;   // 8192
 
 // Workspace header (bytes): [0] error word, [4] scan ticket.
 constexpr size_t kWsHeader = 256;
@@ -148,5 +148,14 @@ __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned lon
 }
 
 __device__ __forceinline__ void set_device_error(int32_t *err, int bits) { atomicOr(err, bits); }
+
+// Programmatic dependent launch: allow the next kernel in the stream (if it
+// was launched with programmatic stream serialization) to start now; wait
+// until the kernel this one depends on has finished and its writes are
+// visible (a no-op when there is no programmatic dependency).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 }  // namespace moe

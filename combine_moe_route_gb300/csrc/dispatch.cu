@@ -41,6 +41,15 @@
 
 #include "launch.h"
 
+// Scatter launch shape (tunable at build time; the defaults are the measured best):
+// warps per block and bulk-copy ring stages per warp.
+#ifndef MOE_SCATTER_WARPS
+#define MOE_SCATTER_WARPS 1
+#endif
+#ifndef MOE_SCATTER_STAGES
+#define MOE_SCATTER_STAGES 3
+#endif
+
 namespace moe {
 
 // --------------------------------------------------------------------------
@@ -53,6 +62,7 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
                                                                  int32_t *__restrict__ local_rank,
                                                                  int32_t *__restrict__ err) {
     extern __shared__ int32_t hist[];   // [kHistWarps][E]
+    pdl_launch_dependents();            // the scan may launch; it waits for this grid's writes
     const int tile = blockIdx.x;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -71,16 +81,19 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
     int e_reg[kItemsPerThread];
     int r_reg[kItemsPerThread];
     int bad = 0;
+    // all of this thread's item loads first, so they are in flight together
 #pragma unroll
     for (int step = 0; step < kItemsPerThread; ++step) {
         const long long i = lo + warp * kItemsPerWarp + step * 32 + lane;
-        int e = -1;
-        if (i < hi) {
-            e = __ldg(topk_idx + i);
-            if (e < 0 || e >= E) {
-                bad = 1;
-                e = -1;
-            }
+        e_reg[step] = (i < hi) ? __ldg(topk_idx + i) : -1;
+    }
+#pragma unroll
+    for (int step = 0; step < kItemsPerThread; ++step) {
+        const long long i = lo + warp * kItemsPerWarp + step * 32 + lane;
+        int e = e_reg[step];
+        if (i < hi && (e < 0 || e >= E)) {
+            bad = 1;
+            e = -1;
         }
         // invalid lanes get distinct negative keys so they never form a group with a valid lane
         const int key = (e >= 0) ? e : -1 - lane;
@@ -157,7 +170,9 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
 
     // virtual block id in start order: every lower id has started, so the
     // lookback below only waits on blocks that are already running
-    if (tid == 0) s_vid = atomicAdd(ticket, 1);
+    pdl_launch_dependents();   // the scatter may launch and stage its first rows
+    if (tid == 0) s_vid = atomicAdd(ticket, 1);   // ticket and flags were cleared before the histogram
+    pdl_wait();                                    // the tile histogram is complete and visible
     __syncthreads();
     const int vid = s_vid;
     const long long base = (long long)vid * kScanChunk + (long long)tid * kScanPerThread;
@@ -238,15 +253,6 @@ struct ScatterArgs {
     int stages;
 };
 
-// Shared memory per stage: the bf16 source row, then (FP8) the e4m3 row and
-// its H/128 scales, then the K destination rows.
-__host__ __device__ inline size_t scatter_stage_bytes(int H, int K, bool fp8) {
-    size_t b = (size_t)H * 2;
-    if (fp8) b += (size_t)H + (size_t)(H / 128) * 4;
-    b += (size_t)K * 4;
-    return (b + 127) & ~(size_t)127;
-}
-
 // 16 lanes quantise one 128-channel block: lane owns 8 consecutive channels.
 __device__ __forceinline__ void quantize_block16(const uint4 xin, uint2 &qout, float &scale_out) {
     const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&xin);
@@ -277,49 +283,72 @@ __device__ __forceinline__ void quantize_block16(const uint4 xin, uint2 &qout, f
     qout.y = w[2] | (w[3] << 16);
 }
 
-// Wait until at most n (0..7) of this thread's committed bulk store groups
-// are still reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_dyn(int n) {
-    switch (n) {
-        case 0: bulk_wait_read<0>(); break;
-        case 1: bulk_wait_read<1>(); break;
-        case 2: bulk_wait_read<2>(); break;
-        case 3: bulk_wait_read<3>(); break;
-        case 4: bulk_wait_read<4>(); break;
-        case 5: bulk_wait_read<5>(); break;
-        case 6: bulk_wait_read<6>(); break;
-        default: bulk_wait_read<7>(); break;
-    }
+// Shared memory of one ring stage: a bf16 source row (H*2 bytes; for FP8 the
+// e4m3 row is written in place over its first H bytes), then for FP8 the
+// row's H/128 scales.
+__host__ __device__ inline size_t scatter_stage_bytes(int H, bool fp8) {
+    size_t b = (size_t)H * 2 + (fp8 ? (size_t)(H / 128) * 4 : 0);
+    return (b + 127) & ~(size_t)127;
 }
 
-// Persistent over tokens g = blockIdx.x + it * gridDim.x.  Thread 0 drives an
-// S-stage ring of bulk copies: the bf16 source row of token it + S - 1 is in
-// flight while token it is copied out.  bf16: the K destination rows are
-// written by bulk stores straight from the staged source row.  FP8: all
-// threads quantise the staged row once (16 lanes per 128-channel block) into
-// an e4m3 row and its scales in shared memory; the e4m3 row leaves by K bulk
-// stores, the scales by plain coalesced stores.
+// Persistent, one warp per token: warp w of the grid takes tokens
+// g = w, w + W, w + 2W, ... (W = warps in the grid) and runs its own ring of
+// S bulk-copy stages, so warps never wait on one another.  Per token:
+//   1. lanes j < K compute the destination row of copy j (scan base of the
+//      token's tile + its in-tile rank) and write tok2row / row2src;
+//   2. wait for the staged source row (mbarrier, bounded);
+//   3. FP8: quantise in place, two 128-channel blocks per step (16 lanes per
+//      block), ascending, so every e4m3 byte lands on bf16 bytes that have
+//      already been read;
+//   4. lane 0 issues K bulk stores of the row (and, when H % 512 == 0, K bulk
+//      stores of the scale row; otherwise the lanes store the scales);
+//   5. once the previous token's stores have read their stage, lane 0 refills
+//      that stage with the token S - 1 ahead.
 template <bool kFp8>
-__global__ void __launch_bounds__(kFp8 ? 256 : 128) scatter_kernel(const ScatterArgs a,
-                                                                    const __grid_constant__ RankTable rt) {
+__global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const ScatterArgs a,
+                                                                         const __grid_constant__ RankTable rt) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) uint64_t full_bar[8];
+    __shared__ __align__(8) uint64_t bars[MOE_SCATTER_WARPS][MOE_SCATTER_STAGES];
+    __shared__ int32_t s_rows[MOE_SCATTER_WARPS][MOE_MAX_TOPK];
+    constexpr int S = MOE_SCATTER_STAGES;
+    static_assert(S >= 2, "the refill schedule needs at least two stages per warp");
 
-    const int tid = threadIdx.x;
-    const int S = a.stages;
-    const int H = a.H;
-    const int K = a.K;
-    const int E = a.E;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = a.H, K = a.K, E = a.E, T = a.T;
     const int nblk = H / 128;
-    const size_t stage_bytes = scatter_stage_bytes(H, K, kFp8);
+    const size_t stage_bytes = scatter_stage_bytes(H, kFp8);
     const uint32_t in_bytes = (uint32_t)H * 2u;
     const uint32_t out_bytes = kFp8 ? (uint32_t)H : in_bytes;
     const size_t recv_pitch = kFp8 ? (size_t)H : (size_t)H * 2;
+    const bool scale_bulk = kFp8 && (nblk * 4) % 16 == 0;
+
+    const long long W = (long long)gridDim.x * MOE_SCATTER_WARPS;
+    const long long gw = (long long)blockIdx.x * MOE_SCATTER_WARPS + warp;
+    const int my_count = (gw < T) ? (int)((T - 1 - gw) / W + 1) : 0;
+    unsigned char *wbase = smem + (size_t)warp * S * stage_bytes;
+    auto stage = [&](int it) { return wbase + (size_t)(it % S) * stage_bytes; };
+    auto token_of = [&](int it) { return gw + (long long)it * W; };
+
+    // prologue: the source rows do not depend on the histogram or the scan,
+    // so their loads go out before waiting for the previous kernel
+    int loads_issued = 0;
+    if (lane == 0 && my_count > 0) {
+        for (int st = 0; st < S; ++st) mbar_init(&bars[warp][st], 1);
+        fence_proxy_async_smem();
+        loads_issued = min(S, my_count);
+        for (int it = 0; it < loads_issued; ++it) {
+            mbar_arrive_expect_tx(&bars[warp][it], in_bytes);
+            bulk_load(stage(it), a.x + token_of(it) * H, in_bytes, &bars[warp][it]);
+        }
+    }
+    __syncwarp();
+    pdl_wait();
 
     // counts / offsets / expert_offsets from the scanned histogram
     {
         const int n = E * rt.R;
-        for (int i = blockIdx.x * blockDim.x + tid; i <= n; i += gridDim.x * blockDim.x) {
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= n; i += gridDim.x * blockDim.x) {
             if (i < n) {
                 const int e = i / rt.R;
                 const int s = i - e * rt.R;
@@ -335,49 +364,20 @@ __global__ void __launch_bounds__(kFp8 ? 256 : 128) scatter_kernel(const Scatter
             }
         }
     }
-
-    const int T = a.T;
-    if ((int)blockIdx.x >= T) return;
-    const int my_count = (T - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
-
-    auto stage_in = [&](int st) { return smem + (size_t)st * stage_bytes; };
-    auto stage_q = [&](int st) { return stage_in(st) + (size_t)H * 2; };
-    auto stage_sc = [&](int st) { return reinterpret_cast<float *>(stage_q(st) + H); };
-    auto stage_rows = [&](int st) {
-        return reinterpret_cast<int32_t *>(stage_in(st) + (size_t)H * 2 +
-                                           (kFp8 ? (size_t)H + (size_t)nblk * 4 : 0));
-    };
-    auto token_of = [&](int it) { return (long long)blockIdx.x + (long long)it * gridDim.x; };
-
-    int loads_issued = 0;   // meaningful in thread 0 only
-    if (tid == 0) {
-        for (int st = 0; st < S; ++st) mbar_init(&full_bar[st], 1);
-        fence_proxy_async_smem();
-    }
-    __syncthreads();
-    if (tid == 0) {
-        const int pre = min(S, my_count);
-        for (int it = 0; it < pre; ++it) {
-            mbar_arrive_expect_tx(&full_bar[it], in_bytes);
-            bulk_load(stage_in(it), a.x + token_of(it) * H, in_bytes, &full_bar[it]);
-        }
-        loads_issued = pre;
-    }
+    if (my_count == 0) return;
 
     int failed_at = -1;
     for (int it = 0; it < my_count; ++it) {
-        const int st = it % S;
         const uint32_t parity = (uint32_t)((it / S) & 1);
-        const long long g = token_of(it);
-        int32_t *rows = stage_rows(st);
-
-        // destination rows of this token's K copies (warp 0, lane j = copy j)
-        if (tid < 32) {
+        unsigned char *buf = stage(it);
+        // 1. destination rows (lane j = copy j)
+        {
+            const long long g = token_of(it);
             const int sidx = upper_bound_minus_one(rt.rank_off, rt.R, (int32_t)g);
             const long long item0 = (long long)rt.rank_off[sidx] * K;
             int e = -1, row = -1;
-            if (tid < K) {
-                const long long i = g * K + tid;
+            if (lane < K) {
+                const long long i = g * K + lane;
                 e = __ldg(a.topk_idx + i);
                 const int lr = a.tok2row[i];
                 if (e >= 0 && e < E && lr >= 0) {
@@ -388,91 +388,81 @@ __global__ void __launch_bounds__(kFp8 ? 256 : 128) scatter_kernel(const Scatter
                     e = -1;
                 }
                 a.tok2row[i] = row;
-                rows[tid] = row;
+                s_rows[warp][lane] = row;
             }
-            int dup = 0;   // the same expert twice in one token
+            int dup = 0;
             for (int j = 0; j < K; ++j) {
                 const int ej = __shfl_sync(0xffffffffu, e, j);
-                if (tid < j && e >= 0 && e == ej) dup = 1;
+                if (lane < j && e >= 0 && e == ej) dup = 1;
             }
-            if (__any_sync(0xffffffffu, dup) && tid == 0) set_device_error(a.err, MOE_DEVERR_DUPLICATE);
+            if (__any_sync(0xffffffffu, dup) && lane == 0) set_device_error(a.err, MOE_DEVERR_DUPLICATE);
         }
 
-        // FP8: the e4m3 row of this stage was last read by the store group of
-        // token it - S; at most S - 1 newer groups may still be reading
-        if (kFp8 && tid == 0 && it >= S) bulk_wait_read_dyn(S - 1);
-        bool ok = mbar_wait_bounded(&full_bar[st], parity);
-        ok = __syncthreads_and(ok);   // also publishes rows[] and orders the buffer reuse above
+        // 2. the staged source row
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][it % S], parity));
         if (!ok) {
-            if (tid == 0) set_device_error(a.err, MOE_DEVERR_COPY_TIMEOUT);
+            if (lane == 0) set_device_error(a.err, MOE_DEVERR_COPY_TIMEOUT);
             failed_at = it;
             break;
         }
 
+        // 3. quantise in place
+        float *sc = reinterpret_cast<float *>(buf + (size_t)H * 2);
         if (kFp8) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(stage_in(st));
-            uint2 *q = reinterpret_cast<uint2 *>(stage_q(st));
-            float *sc = stage_sc(st);
-            const int warp = tid >> 5;
-            const int lane = tid & 31;
-            const int nwarps = blockDim.x >> 5;
+            const uint4 *src = reinterpret_cast<const uint4 *>(buf);
+            uint2 *q = reinterpret_cast<uint2 *>(buf);
             const int hl = lane & 15;
-            for (int b0 = 2 * warp; b0 < nblk; b0 += 2 * nwarps) {   // warp-uniform trip count
+            for (int b0 = 0; b0 < nblk; b0 += 2) {
                 const int b = b0 + (lane >> 4);
                 const bool valid = b < nblk;
                 const uint4 xin = valid ? src[b * 16 + hl] : make_uint4(0u, 0u, 0u, 0u);
                 uint2 qo;
                 float s;
-                quantize_block16(xin, qo, s);
+                quantize_block16(xin, qo, s);   // its shuffles order every lane's read before any write
                 if (valid) {
                     q[b * 16 + hl] = qo;
                     if (hl == 0) sc[b] = s;
                 }
             }
             fence_proxy_async_smem();
-            __syncthreads();
         }
+        __syncwarp();
 
-        if (tid == 0) {
-            const unsigned char *src = kFp8 ? stage_q(st) : stage_in(st);
+        // 4. K bulk stores from the stage
+        if (lane == 0) {
             for (int j = 0; j < K; ++j) {
-                const int row = rows[j];
-                if (row >= 0)
-                    bulk_store(static_cast<unsigned char *>(a.recv_x) + (size_t)row * recv_pitch, src, out_bytes);
+                const int row = s_rows[warp][j];
+                if (row < 0) continue;
+                bulk_store(static_cast<unsigned char *>(a.recv_x) + (size_t)row * recv_pitch, buf, out_bytes);
+                if (scale_bulk) bulk_store(a.recv_scale + (size_t)row * nblk, sc, (uint32_t)nblk * 4u);
             }
             bulk_commit();
-            if (kFp8) {
-                // the staged bf16 row has been consumed by the quantise: refill it now
-                if (it + S < my_count) {
-                    mbar_arrive_expect_tx(&full_bar[st], in_bytes);
-                    bulk_load(stage_in(st), a.x + token_of(it + S) * H, in_bytes, &full_bar[st]);
-                    loads_issued = it + S + 1;
-                }
-            } else if (it >= 1 && it - 1 + S < my_count) {
-                // the previous token's store group has read its stage: refill that stage
-                bulk_wait_read<1>();
-                const int pst = (it - 1) % S;
-                mbar_arrive_expect_tx(&full_bar[pst], in_bytes);
-                bulk_load(stage_in(pst), a.x + token_of(it - 1 + S) * H, in_bytes, &full_bar[pst]);
-                loads_issued = it - 1 + S + 1;
-            }
         }
-        if (kFp8) {
-            const float *sc = stage_sc(st);
-            for (int t = tid; t < K * nblk; t += blockDim.x) {
+        if (kFp8 && !scale_bulk) {
+            for (int t = lane; t < K * nblk; t += 32) {
                 const int j = t / nblk;
                 const int b = t - j * nblk;
-                const int row = rows[j];
+                const int row = s_rows[warp][j];
                 if (row >= 0) a.recv_scale[(size_t)row * nblk + b] = sc[b];
             }
         }
+
+        // 5. refill the previous token's stage once its stores have read it
+        if (lane == 0 && it >= 1 && it - 1 + S < my_count) {
+            bulk_wait_read<1>();
+            const int nxt = it - 1 + S;
+            mbar_arrive_expect_tx(&bars[warp][nxt % S], in_bytes);
+            bulk_load(stage(nxt), a.x + token_of(nxt) * H, in_bytes, &bars[warp][nxt % S]);
+            loads_issued = nxt + 1;
+        }
+        __syncwarp();   // s_rows and the stage are reused S tokens later
     }
 
-    if (tid == 0) {
+    if (lane == 0) {
         if (failed_at >= 0) {
             // let the loads still in flight land before the block's shared memory goes away
             for (int t = failed_at; t < loads_issued; ++t)
-                if (!mbar_wait_bounded(&full_bar[t % S], (uint32_t)((t / S) & 1))) break;
+                if (!mbar_wait_bounded(&bars[warp][t % S], (uint32_t)((t / S) & 1))) break;
         }
         bulk_wait_all();
     }
@@ -535,8 +525,20 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
     if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
 
     const int n = E * rt.ntiles;
-    lookback_scan_kernel<<<p.nscan_blocks, kScanThreads, 0, stream>>>(tile_hist, scan, n, status, ticket, err);
-    if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)p.nscan_blocks);
+        cfg.blockDim = dim3(kScanThreads);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((ce = cudaLaunchKernelEx(&cfg, lookback_scan_kernel, (const int32_t *)tile_hist, scan, n, status, ticket,
+                                     err)) != cudaSuccess)
+            return ce;
+    }
 
     ScatterArgs a;
     a.x = static_cast<const __nv_bfloat16 *>(x);
@@ -555,29 +557,36 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
     a.K = K;
     a.H = H;
 
-    const size_t stage = scatter_stage_bytes(H, K, fp8);
-    const size_t budget = fp8 ? (size_t)100 * 1024 : (size_t)72 * 1024;
-    int stages = (int)(budget / stage);
-    stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
-    a.stages = stages;
-    const size_t smem = stage * stages;
-    const int blocks_per_sm = 2;
-    int grid = sm_count() * blocks_per_sm;
-    const int min_grid = (E * rt.R + 1 + 255) / 256;   // enough threads for the offsets pass
-    if (grid > T) grid = (int)T;
-    if (grid < min_grid) grid = min_grid;
+    const size_t smem = scatter_stage_bytes(H, fp8) * MOE_SCATTER_STAGES * MOE_SCATTER_WARPS;
+    a.stages = MOE_SCATTER_STAGES;
+    const void *kfn = fp8 ? (const void *)scatter_kernel<true> : (const void *)scatter_kernel<false>;
+    if ((ce = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return ce;
+    int per_sm = 0;
+    if ((ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, MOE_SCATTER_WARPS * 32, smem)) !=
+        cudaSuccess)
+        return ce;
+    if (per_sm < 1) per_sm = 1;
+    long long grid = (long long)sm_count() * per_sm;              // persistent: one wave
+    const long long need = (T + MOE_SCATTER_WARPS - 1) / MOE_SCATTER_WARPS;
+    if (grid > need) grid = need;
     if (grid < 1) grid = 1;
-    if (fp8) {
-        if ((ce = cudaFuncSetAttribute(scatter_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem)) != cudaSuccess)
-            return ce;
-        scatter_kernel<true><<<grid, 256, smem, stream>>>(a, rt);
-    } else {
-        if ((ce = cudaFuncSetAttribute(scatter_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem)) != cudaSuccess)
-            return ce;
-        scatter_kernel<false><<<grid, 128, smem, stream>>>(a, rt);
-    }
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(MOE_SCATTER_WARPS * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (fp8)
+        ce = cudaLaunchKernelEx(&cfg, scatter_kernel<true>, a, rt);
+    else
+        ce = cudaLaunchKernelEx(&cfg, scatter_kernel<false>, a, rt);
+    if (ce != cudaSuccess) return ce;
     return cudaGetLastError();
 }
 
