@@ -54,16 +54,23 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link; return the library path.  Skips work when up to date."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          out_dir: str | None = None, defines: tuple[str, ...] = ()) -> str:
+    """Compile and link; return the library path.  Skips work when up to date.
+
+    ``out_dir`` and ``defines`` (``NAME`` or ``NAME=VALUE``) build a separate
+    copy of the library, e.g. one with the test-only hooks switched on; such a
+    build is always redone."""
+    if out_dir is None and not defines and not force and up_to_date():
         return library_path()
-    os.makedirs(OUT_DIR, exist_ok=True)
+    out_dir = out_dir or OUT_DIR
+    os.makedirs(out_dir, exist_ok=True)
     exe = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra += [f"-D{d}" for d in defines]
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [exe, *ARCH, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -76,13 +83,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, log in results:
             if log.strip():
                 print(log, file=sys.stderr)
-    tmp = library_path() + f".tmp{os.getpid()}"
+    target = os.path.join(out_dir, LIB_NAME)
+    tmp = target + f".tmp{os.getpid()}"
     cmd = [exe, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, library_path())
-    return library_path()
+    os.replace(tmp, target)
+    return target
 
 
 if __name__ == "__main__":

@@ -194,11 +194,18 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
         if (lane == kScanThreads / 32 - 1) {
             const int aggregate = wincl;
             int excl = 0;
+#ifdef MOE_TEST_WITHHOLD_SCAN_BLOCK
+            // Test builds only: this block never publishes, so its successor's
+            // bounded lookback runs out (exercises the timeout path).
+            const bool publish = vid != MOE_TEST_WITHHOLD_SCAN_BLOCK;
+#else
+            const bool publish = true;
+#endif
             if (vid == 0) {
                 __threadfence();
-                atomicExch(&status[0], kFlagPrefix | (unsigned long long)(unsigned)aggregate);
+                if (publish) atomicExch(&status[0], kFlagPrefix | (unsigned long long)(unsigned)aggregate);
             } else {
-                atomicExch(&status[vid], kFlagAgg | (unsigned long long)(unsigned)aggregate);
+                if (publish) atomicExch(&status[vid], kFlagAgg | (unsigned long long)(unsigned)aggregate);
                 int p = vid - 1;
                 const uint64_t t0 = global_timer_ns();
                 bool timed_out = false;
@@ -219,7 +226,7 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
                 }
                 if (timed_out) set_device_error(err, MOE_DEVERR_SCAN_TIMEOUT);
                 __threadfence();
-                atomicExch(&status[vid], kFlagPrefix | (unsigned long long)(unsigned)(excl + aggregate));
+                if (publish) atomicExch(&status[vid], kFlagPrefix | (unsigned long long)(unsigned)(excl + aggregate));
             }
             s_excl = excl;
             if ((long long)(vid + 1) * kScanChunk >= n) out[n] = excl + aggregate;   // last block: total
@@ -339,6 +346,11 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
         loads_issued = min(S, my_count);
         for (int it = 0; it < loads_issued; ++it) {
             mbar_arrive_expect_tx(&bars[warp][it], in_bytes);
+#ifdef MOE_TEST_WITHHOLD_FIRST_LOAD
+            // Test builds only: the grid's first warp arms its first stage but never
+            // issues the copy, so its bounded barrier wait runs out.
+            if (gw == 0 && it == 0) continue;
+#endif
             bulk_load(stage(it), a.x + token_of(it) * H, in_bytes, &bars[warp][it]);
         }
     }
@@ -460,9 +472,11 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
 
     if (lane == 0) {
         if (failed_at >= 0) {
-            // let the loads still in flight land before the block's shared memory goes away
+            // let every load this warp issued land before the block's shared
+            // memory goes away (each wait is bounded; one that never arrives
+            // costs its limit and the rest are still waited for)
             for (int t = failed_at; t < loads_issued; ++t)
-                if (!mbar_wait_bounded(&bars[warp][t % S], (uint32_t)((t / S) & 1))) break;
+                (void)mbar_wait_bounded(&bars[warp][t % S], (uint32_t)((t / S) & 1));
         }
         bulk_wait_all();
     }

@@ -6,11 +6,10 @@
 // goes to K routed experts whose outputs are summed with weights.
 //
 // One warp per token.  Lane l holds logits e = l, l+32, l+64, ... in
-// registers.  Each logit becomes a 64-bit key (order-preserving image of the
-// fp32 value in the high word, the complement of the expert id in the low
-// word, so that a larger key means a larger logit and, on equal logits, a
-// smaller id).  K rounds of: per-lane maximum over its not-yet-chosen keys,
-// warp-wide maximum by butterfly shuffles, the owning lane marks the winner.
+// registers as an order-preserving 32-bit image of each fp32 value.  K
+// rounds of: per-lane maximum over its not-yet-chosen keys, warp-wide maximum
+// of the image by one redux.sync, then the smallest expert id among the lanes
+// holding that maximum by a second one; the owning lane marks the winner.
 // The weights are a softmax over the K winners, max-subtracted (the first
 // winner is the largest), exponentials summed in j order, one IEEE division.
 #include "launch.h"
@@ -52,28 +51,29 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
         }
     }
 
+    // K rounds: each lane offers its best remaining key (on equal keys its
+    // lowest slot, i.e. its lowest expert id); the warp keeps the largest key
+    // (one redux.sync) and, among the lanes offering it, the smallest id
+    // (a second redux.sync).
     int my_e = 0;
     uint32_t my_key = 0;
     for (int k = 0; k < K; ++k) {
-        unsigned long long best = 0ull;
+        uint32_t bk = 0u;
+        int bi = -1;
 #pragma unroll
         for (int i = 0; i < NPL; ++i) {
-            if (avail & (1u << i)) {
-                const unsigned long long c =
-                    ((unsigned long long)key[i] << 32) | (unsigned long long)(0xffffffffu - (uint32_t)(lane + 32 * i));
-                best = c > best ? c : best;
+            if ((avail & (1u << i)) && key[i] > bk) {
+                bk = key[i];
+                bi = i;
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
-            best = o > best ? o : best;
-        }
-        const int e_win = (int)(0xffffffffu - (uint32_t)(best & 0xffffffffull));
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t cand = (bi >= 0 && bk == kmax) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+        const int e_win = (int)__reduce_min_sync(0xffffffffu, cand);
         if ((e_win & 31) == lane) avail &= ~(1u << (e_win >> 5));
         if (lane == k) {
             my_e = e_win;
-            my_key = (uint32_t)(best >> 32);
+            my_key = kmax;
         }
     }
 

@@ -1,0 +1,119 @@
+"""Failure detection on the GPU without a fault: the library's bounded device
+waits run out, report MOE_ERR_TIMEOUT through the workspace error word, keep
+every write inside its buffer, and leave the CUDA context usable.
+
+The waits are made to run out by test-only build switches (a flag or a bulk
+copy that nothing ever provides); the product library is built without them.
+  * MOE_TEST_WITHHOLD_SCAN_BLOCK=0: the first lookback-scan block never
+    publishes its status, so the second block's lookback wait ends after its
+    limit (about 2 s) with MOE_DEVERR_SCAN_TIMEOUT.
+  * MOE_TEST_WITHHOLD_FIRST_LOAD: the grid's first scatter warp arms its first
+    stage barrier but never issues the copy, so its wait ends after its limit
+    with MOE_DEVERR_COPY_TIMEOUT."""
+import ctypes
+import time
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+BF16 = 0
+OK, TIMEOUT = 0, 5
+SCAN_TIMEOUT, COPY_TIMEOUT = 0x4, 0x8
+
+
+@pytest.fixture(scope="module")
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from combine_moe_route_gb300 import build
+    build.build()
+    return torch.device("cuda:0")
+
+
+def _hooked_library(tmp_path_factory, define):
+    from combine_moe_route_gb300 import build
+    out = str(tmp_path_factory.mktemp("hooks"))
+    lib = ctypes.CDLL(build.build(out_dir=out, defines=(define,)))
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.moe_dispatch.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.moe_dispatch.restype = i32
+    lib.moe_dispatch_workspace_bytes.argtypes = [i32, i32, i32, i64]
+    lib.moe_dispatch_workspace_bytes.restype = sz
+    lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+    lib.moe_get_device_error.restype = i32
+    return lib
+
+
+def _dispatch_with(lib, x, idx, B, E, dev):
+    T, H = x.shape
+    K = idx.shape[1]
+    R = B.size
+    rows = T * K
+    o = dict(recv=torch.zeros((rows, H), dtype=torch.bfloat16, device=dev),
+             counts=torch.zeros(E * R, dtype=torch.int32, device=dev),
+             offsets=torch.zeros(E * R + 1, dtype=torch.int32, device=dev),
+             eo=torch.zeros(E + 1, dtype=torch.int32, device=dev),
+             tok2row=torch.zeros(rows, dtype=torch.int32, device=dev),
+             row2src=torch.zeros(rows, dtype=torch.int32, device=dev))
+    wsb = lib.moe_dispatch_workspace_bytes(R, E, K, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    t0 = time.perf_counter()
+    st = lib.moe_dispatch(x.data_ptr(), idx.data_ptr(), R, B.ctypes.data, E, K, H, BF16, o["recv"].data_ptr(), None,
+                          o["counts"].data_ptr(), o["offsets"].data_ptr(), o["eo"].data_ptr(),
+                          o["tok2row"].data_ptr(), o["row2src"].data_ptr(), ws.data_ptr(), wsb, stream)
+    assert st == OK                                   # launched fine; the failure is on the device
+    code = ctypes.c_int32(0)
+    dst = lib.moe_get_device_error(ws.data_ptr(), ctypes.byref(code), stream)   # synchronises
+    return dst, code.value, time.perf_counter() - t0, o
+
+
+def _inputs(R, E, K, H, tokens_per_rank, seed, dev):
+    rng = np.random.default_rng(seed)
+    B = np.full(R, tokens_per_rank, np.int32)
+    T = int(B.sum())
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    x = torch.randn(T, H, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16).to(dev)
+    return x, torch.from_numpy(idx).to(dev), B
+
+
+def _context_still_works(x, idx, B, E, oracle):
+    from combine_moe_route_gb300 import binding
+    d = binding.dispatch(x, idx, B, E)
+    st, code = binding.get_device_error(d.workspace)
+    assert st == OK and code == 0
+    ref = oracle.dispatch(x.cpu().view(torch.int16).numpy().view(np.uint16), idx.cpu().numpy(), B, E)
+    assert np.array_equal(d.tok2row.cpu().numpy(), ref["tok2row"])
+    assert np.array_equal(d.recv_x.cpu().view(torch.int16).numpy().view(np.uint16), ref["recv"])
+
+
+def _indices_in_bounds(o, rows):
+    t2r = o["tok2row"].cpu().numpy()
+    r2s = o["row2src"].cpu().numpy()
+    assert np.all((t2r >= -1) & (t2r < rows))
+    assert np.all((r2s >= 0) & (r2s < rows))
+
+
+def test_lookback_wait_runs_out_and_reports(gpu, oracle, tmp_path_factory):
+    lib = _hooked_library(tmp_path_factory, "MOE_TEST_WITHHOLD_SCAN_BLOCK=0")
+    # E = 1024 experts x 16 tiles = 16384 scan elements: two scan blocks
+    x, idx, B = _inputs(8, 1024, 8, 128, 300, 1, gpu)
+    st, code, dt, o = _dispatch_with(lib, x, idx, B, 1024, gpu)
+    assert st == TIMEOUT and (code & SCAN_TIMEOUT), (st, code)
+    assert 1.0 < dt < 60.0                            # the wait ran for its limit, then returned
+    _indices_in_bounds(o, idx.numel())
+    _context_still_works(x, idx, B, 1024, oracle)
+
+
+def test_copy_wait_runs_out_and_reports(gpu, oracle, tmp_path_factory):
+    lib = _hooked_library(tmp_path_factory, "MOE_TEST_WITHHOLD_FIRST_LOAD")
+    x, idx, B = _inputs(2, 8, 2, 256, 40, 2, gpu)
+    st, code, dt, o = _dispatch_with(lib, x, idx, B, 8, gpu)
+    assert st == TIMEOUT and (code & COPY_TIMEOUT), (st, code)
+    assert 1.0 < dt < 60.0
+    t2r = o["tok2row"].cpu().numpy()
+    assert np.all((t2r >= -1) & (t2r < idx.numel()))
+    _context_still_works(x, idx, B, 8, oracle)
