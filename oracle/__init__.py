@@ -70,6 +70,8 @@ def _load():
             lib.oracle_e4m3_decode_array.argtypes = [_u8p, ctypes.c_int64, _f32p]
             lib.oracle_quantize_rows_e4m3.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int, _u8p, _f32p]
             lib.oracle_route_topk.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _f32p]
+            lib.oracle_route_topk_grouped.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                      ctypes.c_int, _i32p, _f32p]
             lib.oracle_dispatch.argtypes = [
                 _u16p, _i32p, ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, _vp, _f32p, _i32p, _i32p, _i32p, _i32p, _i32p]
@@ -152,6 +154,19 @@ def route_topk(logits: np.ndarray, K: int):
     idx = np.empty((T, K), np.int32)
     w = np.empty((T, K), np.float32)
     _load().oracle_route_topk(_ptr(logits, _f32p), T, E, K, _ptr(idx, _i32p), _ptr(w, _f32p))
+    return idx, w
+
+
+def route_topk_grouped(logits: np.ndarray, K: int, n_groups: int, topk_groups: int):
+    """Group-limited top-K: best ``topk_groups`` of ``n_groups`` groups by their largest logit,
+    then top-K among their experts; weights as in ``route_topk``."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    assert E % n_groups == 0 and 1 <= topk_groups <= n_groups and 1 <= K <= topk_groups * (E // n_groups)
+    idx = np.empty((T, K), np.int32)
+    w = np.empty((T, K), np.float32)
+    _load().oracle_route_topk_grouped(_ptr(logits, _f32p), T, E, K, n_groups, topk_groups, _ptr(idx, _i32p),
+                                      _ptr(w, _f32p))
     return idx, w
 
 

@@ -32,6 +32,7 @@
  *   oracle_bf16_from_f32 / oracle_f32_from_bf16   pinned (library cast, IEEE cases)
  *   oracle_e4m3_decode / oracle_e4m3_encode       pinned (library cast, OCP table)
  *   oracle_route_topk                             pinned (argmax, full sort, brute force, softmax)
+ *   oracle_route_topk_grouped                     pinned (one group / all groups = plain route, library sort)
  *   oracle_dispatch                               pinned (library stable sort, brute force, invariants)
  *   oracle_expert_scale                           pinned (library arithmetic)
  *   oracle_combine / oracle_combine_f64           pinned (identity experts, one-hot, error bound)
@@ -148,6 +149,74 @@ void oracle_route_topk(const float *logits, int T, int E, int K,
             topk_w[(size_t)g * K + j] = (float)(ex[j] / sum);
     }
     free(chosen);
+    free(ex);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Group-limited route: [DSD] "MoE router" (DeepSeek's routing takes a group  */
+/* top-K first; Mixtral's routing is the special case where the group top-K  */
+/* is the group of all experts).  Reading (the page gives no formula): the E  */
+/* experts form n_groups contiguous groups of E/n_groups; a group's score is  */
+/* its largest logit; the topk_groups best groups are kept (equal scores ->   */
+/* smaller group id); then the K largest logits among the kept groups' experts */
+/* are chosen exactly as in oracle_route_topk, and weighted the same way.     */
+/* ------------------------------------------------------------------------ */
+void oracle_route_topk_grouped(const float *logits, int T, int E, int K, int n_groups, int topk_groups,
+                               int32_t *topk_idx, float *topk_w)
+{
+    int gs = E / n_groups;
+    unsigned char *allowed = (unsigned char *)malloc((size_t)(E > 0 ? E : 1));
+    unsigned char *chosen = (unsigned char *)malloc((size_t)(E > 0 ? E : 1));
+    unsigned char *gkept = (unsigned char *)malloc((size_t)(n_groups > 0 ? n_groups : 1));
+    float *gscore = (float *)malloc(sizeof(float) * (size_t)(n_groups > 0 ? n_groups : 1));
+    double *ex = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    for (int g = 0; g < T; ++g) {
+        const float *l = logits + (size_t)g * E;
+        /* 1. group scores */
+        for (int q = 0; q < n_groups; ++q) {
+            float m = l[q * gs];
+            for (int e = q * gs + 1; e < (q + 1) * gs; ++e)
+                if (l[e] > m) m = l[e];
+            gscore[q] = m;
+            gkept[q] = 0;
+        }
+        /* 2. keep the topk_groups best groups */
+        for (int r = 0; r < topk_groups; ++r) {
+            int best = -1;
+            for (int q = 0; q < n_groups; ++q) {
+                if (gkept[q]) continue;
+                if (best < 0 || gscore[q] > gscore[best]) best = q;
+            }
+            gkept[best] = 1;
+        }
+        for (int e = 0; e < E; ++e) {
+            allowed[e] = gkept[e / gs];
+            chosen[e] = 0;
+        }
+        /* 3. top-K among the allowed experts */
+        for (int j = 0; j < K; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (!allowed[e] || chosen[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e;
+            }
+            chosen[best] = 1;
+            topk_idx[(size_t)g * K + j] = best;
+        }
+        /* 4. softmax over the chosen logits (fp64, rounded once) */
+        double m = (double)l[topk_idx[(size_t)g * K]];
+        double sum = 0.0;
+        for (int j = 0; j < K; ++j) {
+            ex[j] = exp((double)l[topk_idx[(size_t)g * K + j]] - m);
+            sum += ex[j];
+        }
+        for (int j = 0; j < K; ++j)
+            topk_w[(size_t)g * K + j] = (float)(ex[j] / sum);
+    }
+    free(allowed);
+    free(chosen);
+    free(gkept);
+    free(gscore);
     free(ex);
 }
 

@@ -358,3 +358,40 @@ def test_full_layer_invariants_workload_toy(oracle):
     x = wl.bf16_bits(inp["x"])
     d = oracle.layer(x, inp["logits"], inp["B"], 16, 2)
     _check_dispatch_invariants(d, d["topk_idx"], inp["B"], 16, x)
+
+
+# --------------------------------------------------------------------------
+# group-limited route
+# --------------------------------------------------------------------------
+
+def test_grouped_route_one_group_or_all_groups_is_plain_route(oracle):
+    # the MoE-router section: plain (Mixtral) routing is the case where the group
+    # top-K covers every expert
+    rng = np.random.default_rng(20)
+    for lg in (_tie_logits(300, 64, 21), rng.standard_normal((300, 256)).astype(np.float32)):
+        E = lg.shape[1]
+        for K in (1, 2, 8):
+            idx, w = oracle.route_topk(lg, K)
+            for G, M in ((1, 1), (8, 8), (4, 4)):
+                gi, gw = oracle.route_topk_grouped(lg, K, G, M)
+                assert np.array_equal(gi, idx) and np.array_equal(gw, w)
+
+
+def test_grouped_route_matches_library_sort(oracle):
+    rng = np.random.default_rng(22)
+    for lg in (_tie_logits(200, 32, 23), rng.standard_normal((200, 64)).astype(np.float32)):
+        T, E = lg.shape
+        for G, M, K in ((8, 4, 8), (4, 1, 2), (8, 3, 5), (2, 1, 1)):
+            gs = E // G
+            gi, gw = oracle.route_topk_grouped(lg, K, G, M)
+            for g in range(T):
+                gmax = lg[g].reshape(G, gs).max(axis=1)
+                keep = np.lexsort((np.arange(G), -gmax))[:M]          # score desc, id asc
+                allowed = np.isin(np.arange(E) // gs, keep)
+                cand = np.nonzero(allowed)[0]
+                order = cand[np.lexsort((cand, -lg[g, cand]))][:K]
+                assert np.array_equal(gi[g], order)
+                assert len(set(gi[g] // gs)) <= M
+            sel = np.take_along_axis(lg, gi, axis=1).astype(np.float64)
+            ref = scipy.special.softmax(sel, axis=1)
+            assert np.all(np.abs(gw - ref) <= 2.0**-24 * np.maximum(ref, 2.0**-126) * 2)
