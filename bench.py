@@ -188,6 +188,21 @@ def barrier(world: int):
         dist.barrier()
 
 
+def time_call(fn, stream, reps: int = 50) -> float:
+    """Mean µs of fn() over reps calls, CUDA events on the launching stream, after 3 warm-ups."""
+    for _ in range(3):
+        fn()
+    a = torch.cuda.Event(enable_timing=True)
+    z = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    z.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(z) * 1e3 / reps
+
+
 def replica_value(per_rank_us: float, world: int) -> float:
     """Whole-job µs per layer for N independent replicas: the slowest rank's
     time per layer divided by the N layers processed in that time."""
@@ -403,6 +418,18 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     e2e_us = max_over_ranks(e0.elapsed_time(e1) * 1e3 / e2e_steps, world, dev)
 
+    # the "next" rows, each timed on its own after the main region (not part of value)
+    next_rows = {}
+    if E % 8 == 0 and K <= 4 * (E // 8):
+        g_idx = torch.empty_like(idx)
+        g_w = torch.empty_like(wts)
+
+        def grouped():
+            b.route_topk_grouped(logits, K, 8, 4, topk_idx=g_idx, topk_w=g_w)
+
+        us = time_call(grouped, stream, reps=50)
+        next_rows["route_grouped_G8_M4"] = {"us": us, "GBps": route_bytes(T, E, K) / (us * 1e-6) / 1e9}
+
     # correctness of what was timed: the last step's outputs equal the first layer's
     st, code = b.get_device_error(d.workspace)
     if st != 0:
@@ -466,6 +493,7 @@ def run_ours(args, world, rank, local):
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"], "window": clk["window"]},
         "cpu_baseline": cpu,
+        "next_rows": next_rows,
     }
     if line_note:
         line["note"] = line_note

@@ -58,6 +58,8 @@ def load_library() -> ctypes.CDLL:
         lib.moe_strerror.restype = ctypes.c_char_p
         lib.moe_route_topk.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         lib.moe_route_topk.restype = i32
+        lib.moe_route_topk_grouped.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp]
+        lib.moe_route_topk_grouped.restype = i32
         lib.moe_dispatch_workspace_bytes.argtypes = [i32, i32, i32, i64]
         lib.moe_dispatch_workspace_bytes.restype = sz
         lib.moe_dispatch.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -129,6 +131,28 @@ def route_topk(logits: torch.Tensor, K: int, *, topk_idx: torch.Tensor | None = 
     with torch.cuda.device(dev):
         _check(load_library().moe_route_topk(_ptr(logits), T, E, K, _ptr(topk_idx), _ptr(topk_w),
                                              _stream_handle(stream, dev)), "moe_route_topk")
+    return topk_idx, topk_w
+
+
+def route_topk_grouped(logits: torch.Tensor, K: int, n_groups: int, topk_groups: int, *,
+                       topk_idx: torch.Tensor | None = None, topk_w: torch.Tensor | None = None, stream=None):
+    """Group-limited top-K: keep the ``topk_groups`` best of ``n_groups`` contiguous expert
+    groups (by their largest logit), then top-K among their experts."""
+    _dev(logits, "logits", torch.float32)
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T, E]")
+    T, E = logits.shape
+    dev = logits.device
+    if topk_idx is None:
+        topk_idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, K), dtype=torch.float32, device=dev)
+    _dev(topk_idx, "topk_idx", torch.int32, (T, K))
+    _dev(topk_w, "topk_w", torch.float32, (T, K))
+    with torch.cuda.device(dev):
+        _check(load_library().moe_route_topk_grouped(_ptr(logits), T, E, K, n_groups, topk_groups, _ptr(topk_idx),
+                                                     _ptr(topk_w), _stream_handle(stream, dev)),
+               "moe_route_topk_grouped")
     return topk_idx, topk_w
 
 

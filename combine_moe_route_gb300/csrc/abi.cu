@@ -65,7 +65,19 @@ moe_status moe_route_topk(const float *logits, int T, int E, int K, int32_t *top
     if ((long long)T * E >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
-    return cuda_status(moe::launch_route_topk(logits, T, E, K, topk_idx, topk_w, (cudaStream_t)stream));
+    return cuda_status(moe::launch_route_topk(logits, T, E, K, 1, 1, topk_idx, topk_w, (cudaStream_t)stream));
+}
+
+moe_status moe_route_topk_grouped(const float *logits, int T, int E, int K, int n_groups, int topk_groups,
+                                  int32_t *topk_idx, float *topk_w, moe_stream_t stream) {
+    if (T < 0 || !topk_shape_ok(E, K)) return MOE_ERR_INVALID_ARG;
+    if (n_groups < 1 || n_groups > MOE_MAX_GROUPS || E % n_groups != 0) return MOE_ERR_INVALID_ARG;
+    if (topk_groups < 1 || topk_groups > n_groups || K > topk_groups * (E / n_groups)) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * E >= (1ll << 40)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_route_topk(logits, T, E, K, n_groups, topk_groups, topk_idx, topk_w,
+                                              (cudaStream_t)stream));
 }
 
 size_t moe_dispatch_workspace_bytes(int R, int E, int K, int64_t T) {

@@ -22,8 +22,8 @@ DispatchPlan plan_dispatch(int E, int ntiles);
 int max_tiles(int R, int K, long long T);
 int device_sm_count();
 
-cudaError_t launch_route_topk(const float *logits, int T, int E, int K, int32_t *topk_idx, float *topk_w,
-                              cudaStream_t stream);
+cudaError_t launch_route_topk(const float *logits, int T, int E, int K, int G, int M, int32_t *topk_idx,
+                              float *topk_w, cudaStream_t stream);
 cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
                             bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *offsets,
                             int32_t *expert_offsets, int32_t *tok2row, int32_t *row2src, void *workspace,

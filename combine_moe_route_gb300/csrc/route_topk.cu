@@ -28,10 +28,20 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
     return __uint_as_float(u);
 }
 
+constexpr int kRouteThreads = 256;
+
+// G > 1: group-limited routing (Perplexity, "Lower latency and higher
+// throughput with multi-node DeepSeek deployment", "MoE router": DeepSeek's
+// group top-K, of which the plain top-K is the one-group case).  The E experts
+// form G contiguous groups; a group scores its largest logit; the M best
+// groups are kept (equal scores: smaller group id) and only their experts
+// stay eligible for the K rounds.
 template <int NPL>   // logits per lane: E <= 32 * NPL
-__global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict__ logits, int T, int E, int K,
-                                                         int32_t *__restrict__ topk_idx,
-                                                         float *__restrict__ topk_w) {
+__global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(const float *__restrict__ logits, int T, int E,
+                                                                   int K, int G, int M,
+                                                                   int32_t *__restrict__ topk_idx,
+                                                                   float *__restrict__ topk_w) {
+    __shared__ uint32_t s_gmax[kRouteThreads / 32][32];
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
     const long long g = (long long)blockIdx.x * warps + (threadIdx.x >> 5);
@@ -55,6 +65,29 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
     // lowest slot, i.e. its lowest expert id); the warp keeps the largest key
     // (one redux.sync) and, among the lanes offering it, the smallest id
     // (a second redux.sync).
+    if (G > 1) {
+        uint32_t *gm = s_gmax[threadIdx.x >> 5];
+        const int gs = E / G;
+        if (lane < G) gm[lane] = 0u;
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+            if (avail & (1u << i)) atomicMax(&gm[(lane + 32 * i) / gs], key[i]);
+        __syncwarp();
+        const uint32_t gkey = (lane < G) ? gm[lane] : 0u;   // every real group's key is > 0
+        bool open = lane < G;
+        uint32_t kept = 0u;
+        for (int r = 0; r < M; ++r) {
+            const uint32_t gmax = __reduce_max_sync(0xffffffffu, open ? gkey : 0u);
+            const uint32_t gwin = __reduce_min_sync(0xffffffffu, (open && gkey == gmax) ? (uint32_t)lane : 0xffffffffu);
+            kept |= 1u << gwin;
+            if ((uint32_t)lane == gwin) open = false;
+        }
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+            if (!((kept >> ((lane + 32 * i) / gs)) & 1u)) avail &= ~(1u << i);
+    }
+
     int my_e = 0;
     uint32_t my_key = 0;
     for (int k = 0; k < K; ++k) {
@@ -89,25 +122,27 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float *__restrict
     }
 }
 
-cudaError_t launch_route_topk(const float *logits, int T, int E, int K, int32_t *topk_idx, float *topk_w,
-                              cudaStream_t stream) {
-    constexpr int kThreads = 256;
-    const int warps = kThreads / 32;
+cudaError_t launch_route_topk(const float *logits, int T, int E, int K, int G, int M, int32_t *topk_idx,
+                              float *topk_w, cudaStream_t stream) {
+    const int warps = kRouteThreads / 32;
     const unsigned grid = (unsigned)((T + warps - 1) / warps);
+#define MOE_ROUTE_LAUNCH(NPL) \
+    route_topk_kernel<NPL><<<grid, kRouteThreads, 0, stream>>>(logits, T, E, K, G, M, topk_idx, topk_w)
     if (E <= 32)
-        route_topk_kernel<1><<<grid, kThreads, 0, stream>>>(logits, T, E, K, topk_idx, topk_w);
+        MOE_ROUTE_LAUNCH(1);
     else if (E <= 64)
-        route_topk_kernel<2><<<grid, kThreads, 0, stream>>>(logits, T, E, K, topk_idx, topk_w);
+        MOE_ROUTE_LAUNCH(2);
     else if (E <= 128)
-        route_topk_kernel<4><<<grid, kThreads, 0, stream>>>(logits, T, E, K, topk_idx, topk_w);
+        MOE_ROUTE_LAUNCH(4);
     else if (E <= 256)
-        route_topk_kernel<8><<<grid, kThreads, 0, stream>>>(logits, T, E, K, topk_idx, topk_w);
+        MOE_ROUTE_LAUNCH(8);
     else if (E <= 384)
-        route_topk_kernel<12><<<grid, kThreads, 0, stream>>>(logits, T, E, K, topk_idx, topk_w);
+        MOE_ROUTE_LAUNCH(12);
     else if (E <= 512)
-        route_topk_kernel<16><<<grid, kThreads, 0, stream>>>(logits, T, E, K, topk_idx, topk_w);
+        MOE_ROUTE_LAUNCH(16);
     else
-        route_topk_kernel<32><<<grid, kThreads, 0, stream>>>(logits, T, E, K, topk_idx, topk_w);
+        MOE_ROUTE_LAUNCH(32);
+#undef MOE_ROUTE_LAUNCH
     return cudaGetLastError();
 }
 

@@ -63,6 +63,7 @@ extern "C" {
 #define MOE_MAX_EXPERTS 1024   /* E */
 #define MOE_MAX_TOPK 32        /* K */
 #define MOE_MAX_HIDDEN 16384   /* H */
+#define MOE_MAX_GROUPS 32      /* expert groups of moe_route_topk_grouped */
 
 /* A CUDA stream (the same type as cudaStream_t); NULL is the legacy default stream. */
 typedef struct CUstream_st *moe_stream_t;
@@ -114,6 +115,26 @@ MOE_API const char *moe_strerror(int status);
  */
 MOE_API moe_status moe_route_topk(const float *logits, int T, int E, int K,
                           int32_t *topk_idx, float *topk_w, moe_stream_t stream);
+
+/*
+ * moe_route_topk_grouped -- group-limited top-K ([DSD] "MoE router": DeepSeek's
+ * routing takes a group top-K first; Mixtral's is the special case where the
+ * group top-K is the group of all experts).  The page gives no formula; the
+ * reading implemented is: the E experts form n_groups contiguous groups of
+ * E/n_groups; a group's score is its largest logit; the topk_groups best
+ * groups are kept (equal scores go to the smaller group id); then the K
+ * largest logits among the kept groups' experts are chosen and weighted
+ * exactly as by moe_route_topk.  With n_groups == 1, or topk_groups ==
+ * n_groups, the result equals moe_route_topk's.  With groups aligned to ranks
+ * (n_groups = R) every token reaches at most topk_groups ranks.
+ *
+ *   n_groups    1..MOE_MAX_GROUPS, dividing E.
+ *   topk_groups 1..n_groups, with K <= topk_groups * (E / n_groups).
+ *   other arguments, outputs and errors as moe_route_topk.
+ */
+MOE_API moe_status moe_route_topk_grouped(const float *logits, int T, int E, int K, int n_groups,
+                                          int topk_groups, int32_t *topk_idx, float *topk_w,
+                                          moe_stream_t stream);
 
 /*
  * Bytes of device workspace moe_dispatch needs for these sizes (an upper bound

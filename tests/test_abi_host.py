@@ -154,3 +154,18 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         binding.combine(torch.zeros(8, 16, dtype=torch.bfloat16), torch.zeros(8, dtype=torch.int32),
                         torch.zeros(4, 2))
+
+
+def test_route_grouped_validation(lib):
+    f = lib.moe_route_topk_grouped
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(FAKE, 4, 256, 8, 0, 1, FAKE, FAKE, None) == INVALID       # no groups
+    assert f(FAKE, 4, 256, 8, 33, 1, FAKE, FAKE, None) == INVALID      # more than 32 groups
+    assert f(FAKE, 4, 256, 8, 6, 1, FAKE, FAKE, None) == INVALID       # does not divide E
+    assert f(FAKE, 4, 256, 8, 8, 0, FAKE, FAKE, None) == INVALID       # no kept group
+    assert f(FAKE, 4, 256, 8, 8, 9, FAKE, FAKE, None) == INVALID       # more kept than groups
+    assert f(FAKE, 4, 64, 9, 8, 1, FAKE, FAKE, None) == INVALID        # K > kept experts (8)
+    assert f(None, 4, 256, 8, 8, 4, FAKE, FAKE, None) == INVALID
+    assert f(None, 0, 256, 8, 8, 4, None, None, None) == OK

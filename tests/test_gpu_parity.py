@@ -130,6 +130,31 @@ def test_workload_end_to_end(case, oracle):
     assert np.all(np.abs(got - want) <= tol)
 
 
+@pytest.mark.parametrize("E,K,G,M,T", [
+    (256, 8, 8, 4, 32768),     # DeepSeek-V3-like grouping on the prefill layer's token count
+    (256, 8, 1, 1, 4096),      # one group: plain routing
+    (256, 8, 8, 8, 4096),      # every group kept: plain routing
+    (384, 8, 32, 3, 2048),     # 32 groups of 12
+    (64, 6, 16, 2, 1000),      # 16 groups of 4, K = 6 of the 8 kept experts
+    (1024, 32, 32, 32, 256),   # limits
+])
+def test_route_grouped(E, K, G, M, T, gpu, oracle):
+    b = _binding()
+    rng = np.random.default_rng(E + K + G + M)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[: T // 4] = np.round(logits[: T // 4])              # many exact ties in a quarter of the rows
+    lg = torch.from_numpy(logits).to(gpu)
+    idx, w = b.route_topk_grouped(lg, K, G, M)
+    torch.cuda.synchronize()
+    o_idx, o_w = oracle.route_topk_grouped(logits, K, G, M)
+    assert np.array_equal(i32(idx), o_idx)
+    sel = np.take_along_axis(logits, o_idx, axis=1)
+    assert np.all(np.abs(f32(w).astype(np.float64) - o_w) <= weight_tolerance(o_w, sel, K))
+    if G == 1 or M == G:
+        p_idx, p_w = b.route_topk(lg, K)
+        assert torch.equal(p_idx, idx) and torch.equal(p_w, w)
+
+
 # ---------------------------------------------------------------------------
 # random small shapes, ragged tails, edge cases
 # ---------------------------------------------------------------------------
