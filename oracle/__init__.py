@@ -76,6 +76,12 @@ def _load():
                 _u16p, _i32p, ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, _vp, _f32p, _i32p, _i32p, _i32p, _i32p, _i32p]
             lib.oracle_dispatch.restype = ctypes.c_int
+            lib.oracle_dispatch_ll.argtypes = [
+                _u16p, _i32p, ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, _vp, _f32p, _i32p, _i32p, _i32p]
+            lib.oracle_dispatch_ll.restype = ctypes.c_int
+            lib.oracle_combine_ll_push.argtypes = [_u16p, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, _u16p]
             lib.oracle_expert_scale.argtypes = [
                 _vp, _f32p, ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16p]
             lib.oracle_combine.argtypes = [
@@ -206,6 +212,48 @@ def dispatch(x_bf16: np.ndarray, topk_idx: np.ndarray, B, E: int, fp8: bool = Fa
         raise ValueError("oracle_dispatch: expert index out of range")
     return dict(recv=recv, recv_scale=recv_scale, counts=counts, offsets=offsets,
                 expert_offsets=expert_offsets, tok2row=tok2row, row2src=row2src)
+
+
+def dispatch_ll(x_bf16: np.ndarray, topk_idx: np.ndarray, B, E: int, C: int, fp8: bool = False) -> dict:
+    """Low-latency layout: copy j of token g of rank s goes to row (e*R + s)*C + slot of an
+    [E*R*C, H] rectangle.  Rows past counts[e*R+s] in a region stay zero here.  Returns recv,
+    recv_scale, counts [E*R], tok2row [T*K], row2src [E*R*C] (-1 where unfilled)."""
+    x = _c(x_bf16, np.uint16)
+    idx = _c(topk_idx, np.int32)
+    B = _c(B, np.int32)
+    R = B.size
+    T, H = x.shape
+    K = idx.shape[1] if idx.ndim == 2 else (idx.size // T if T else 0)
+    rows = E * R * C
+    if fp8:
+        recv = np.zeros((rows, H), np.uint8)
+        recv_scale = np.zeros((rows, H // 128), np.float32)
+    else:
+        recv = np.zeros((rows, H), np.uint16)
+        recv_scale = None
+    counts = np.empty(E * R, np.int32)
+    tok2row = np.empty(T * K, np.int32)
+    row2src = np.full(rows, -1, np.int32)
+    rc = _load().oracle_dispatch_ll(
+        _ptr(x, _u16p), _ptr(idx.reshape(-1), _i32p), R, _ptr(B, _i32p), E, K, H, C, int(bool(fp8)),
+        recv.ctypes.data_as(_vp), _ptr(recv_scale, _f32p), _ptr(counts, _i32p), _ptr(tok2row, _i32p),
+        _ptr(row2src, _i32p))
+    if rc == -1:
+        raise ValueError("oracle_dispatch_ll: expert index out of range")
+    if rc == -2:
+        raise ValueError("oracle_dispatch_ll: a rank holds more tokens than the chunk cap C")
+    return dict(recv=recv, recv_scale=recv_scale, counts=counts, tok2row=tok2row, row2src=row2src)
+
+
+def combine_ll_push(y_bf16: np.ndarray, row2src: np.ndarray, counts: np.ndarray, R: int, E: int, C: int,
+                    T: int, K: int) -> np.ndarray:
+    """Push each filled rectangle row to its origin slot: ret [T*K, H] (bf16 bits)."""
+    y = _c(y_bf16, np.uint16)
+    H = y.shape[1]
+    ret = np.zeros((T * K, H), np.uint16)
+    _load().oracle_combine_ll_push(_ptr(y, _u16p), _ptr(_c(row2src, np.int32), _i32p),
+                                   _ptr(_c(counts, np.int32), _i32p), R, E, C, H, _ptr(ret, _u16p))
+    return ret
 
 
 def expert_scale(recv: np.ndarray, recv_scale, expert_offsets: np.ndarray, E: int,

@@ -34,6 +34,7 @@
  *   oracle_route_topk                             pinned (argmax, full sort, brute force, softmax)
  *   oracle_route_topk_grouped                     pinned (one group / all groups = plain route, library sort)
  *   oracle_dispatch                               pinned (library stable sort, brute force, invariants)
+ *   oracle_dispatch_ll / oracle_combine_ll_push   pinned (same slots and payload as the ragged layout)
  *   oracle_expert_scale                           pinned (library arithmetic)
  *   oracle_combine / oracle_combine_f64           pinned (identity experts, one-hot, error bound)
  */
@@ -323,6 +324,80 @@ int oracle_dispatch(const uint16_t *x, const int32_t *topk_idx,
     free(qrow);
     free(srow);
     return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Low-latency dispatch: [EPK] "Optimising for latency: send without asking"  */
+/* (a fixed private region per (source rank, expert) pair, sized for the     */
+/* worst case, so the write address is a static formula -- no prefix sum over */
+/* actual counts -- with the tokens a rank may dispatch per call capped at a  */
+/* fixed chunk size C).                                                       */
+/* Row of copy j of token g = (e*R + s)*C + slot, where s is g's rank and     */
+/* slot counts the earlier tokens of rank s routed to e (ascending t, as in   */
+/* the throughput layout).  recv has E*R*C rows; rows past counts[e*R+s] in a */
+/* region are left untouched.  Requires B[s] <= C.  Returns 0, -1 for an      */
+/* expert index out of range, -2 for B[s] > C.                                */
+/* ------------------------------------------------------------------------ */
+int oracle_dispatch_ll(const uint16_t *x, const int32_t *topk_idx,
+                       int R, const int32_t *B, int E, int K, int H, int C, int recv_fp8,
+                       void *recv, float *recv_scale, int32_t *counts,
+                       int32_t *tok2row, int32_t *row2src)
+{
+    int64_t T = 0;
+    for (int s = 0; s < R; ++s) {
+        if (B[s] > C) return -2;
+        T += B[s];
+    }
+    for (int64_t i = 0; i < T * K; ++i)
+        if (topk_idx[i] < 0 || topk_idx[i] >= E) return -1;
+    for (int i = 0; i < E * R; ++i) counts[i] = 0;   /* doubles as the per-region cursor */
+    uint8_t *qrow = NULL;
+    float *srow = NULL;
+    if (recv_fp8) {
+        qrow = (uint8_t *)malloc((size_t)H);
+        srow = (float *)malloc(sizeof(float) * (size_t)(H / 128 > 0 ? H / 128 : 1));
+    }
+    int64_t g = 0;
+    for (int s = 0; s < R; ++s) {
+        for (int t = 0; t < B[s]; ++t, ++g) {
+            const uint16_t *xrow = x + g * (int64_t)H;
+            if (recv_fp8) quantize_row_e4m3(xrow, H, qrow, srow);
+            for (int j = 0; j < K; ++j) {
+                int e = topk_idx[g * K + j];
+                int32_t slot = counts[e * R + s]++;
+                int64_t row = ((int64_t)e * R + s) * C + slot;
+                tok2row[g * K + j] = (int32_t)row;
+                row2src[row] = (int32_t)(g * K + j);
+                if (recv_fp8) {
+                    memcpy((uint8_t *)recv + row * H, qrow, (size_t)H);
+                    memcpy(recv_scale + row * (H / 128), srow, sizeof(float) * (size_t)(H / 128));
+                } else {
+                    memcpy((uint16_t *)recv + row * H, xrow, sizeof(uint16_t) * (size_t)H);
+                }
+            }
+        }
+    }
+    free(qrow);
+    free(srow);
+    return 0;
+}
+
+/* Push-style return of the low-latency layout ([EPK] "Optimising for        */
+/* latency": dispatch tagged every token with where it came from, so the     */
+/* expert's host writes each output straight to a private slot on the token's */
+/* origin rank, indexed by the token's position there and by which of its K   */
+/* experts this is).  ret[g*K + j] = y[row] for every filled row of the       */
+/* rectangle (row2src[row] = g*K + j).  The origin then forms                 */
+/* out[g] = sum_j w[g,j] * ret[g*K + j] (oracle_combine with tok2row = id).   */
+void oracle_combine_ll_push(const uint16_t *y, const int32_t *row2src, const int32_t *counts,
+                            int R, int E, int C, int H, uint16_t *ret)
+{
+    for (int e = 0; e < E; ++e)
+        for (int s = 0; s < R; ++s)
+            for (int slot = 0; slot < counts[e * R + s]; ++slot) {
+                int64_t row = ((int64_t)e * R + s) * C + slot;
+                memcpy(ret + (int64_t)row2src[row] * H, y + row * H, sizeof(uint16_t) * (size_t)H);
+            }
 }
 
 /* ------------------------------------------------------------------------ */

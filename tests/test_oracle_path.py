@@ -395,3 +395,66 @@ def test_grouped_route_matches_library_sort(oracle):
             sel = np.take_along_axis(lg, gi, axis=1).astype(np.float64)
             ref = scipy.special.softmax(sel, axis=1)
             assert np.all(np.abs(gw - ref) <= 2.0**-24 * np.maximum(ref, 2.0**-126) * 2)
+
+
+# --------------------------------------------------------------------------
+# low-latency (fixed-rectangle) layout
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("R,E,K,H,B,C,fp8", [
+    (8, 16, 2, 256, [5, 0, 17, 3, 64, 1, 9, 2], 64, False),
+    (4, 32, 8, 256, [7, 0, 3, 12], 12, True),
+    (2, 8, 8, 128, [16, 16], 16, False),          # K == E: every expert gets every token
+    (3, 9, 3, 64, [0, 0, 0], 4, False),           # empty
+])
+def test_ll_layout_is_the_ragged_layout_in_fixed_regions(oracle, R, E, K, H, B, C, fp8):
+    rng = np.random.default_rng(30 + K)
+    B = np.asarray(B, np.int32)
+    T = int(B.sum())
+    idx = _random_routing(T, E, K, rng) if T else np.zeros((0, K), np.int32)
+    x = oracle.bf16_from_f32(rng.standard_normal((T, H)).astype(np.float32))
+    ll = oracle.dispatch_ll(x, idx, B, E, C, fp8=fp8)
+    rg = oracle.dispatch(x, idx, B, E, fp8=fp8)
+    assert np.array_equal(ll["counts"], rg["counts"])
+    # copy j of token g: same (expert, rank) region, same slot as its place in the ragged segment
+    ragged = rg["tok2row"]
+    region = ll["tok2row"] // C
+    slot = ll["tok2row"] % C
+    flat = idx.reshape(-1)
+    src_rank = np.repeat(np.arange(R), B * K)
+    assert np.array_equal(region, flat * R + src_rank)
+    assert np.array_equal(slot, ragged - rg["offsets"][flat * R + src_rank])
+    assert np.all(slot < np.maximum(B[src_rank], 1))
+    # payload and source tags of every filled row
+    filled = ll["row2src"] >= 0
+    assert filled.sum() == T * K
+    assert np.array_equal(ll["recv"][ll["tok2row"]], rg["recv"][ragged])
+    if fp8:
+        assert np.array_equal(ll["recv_scale"][ll["tok2row"]], rg["recv_scale"][ragged])
+    assert np.array_equal(ll["row2src"][ll["tok2row"]], np.arange(T * K))
+
+
+def test_ll_rejects_more_tokens_than_the_chunk_cap(oracle):
+    with pytest.raises(ValueError):
+        oracle.dispatch_ll(np.zeros((5, 8), np.uint16), np.zeros((5, 1), np.int32), [5], 2, 4)
+
+
+def test_ll_push_then_reduce_equals_gather(oracle):
+    rng = np.random.default_rng(31)
+    R, E, K, H, C = 4, 16, 4, 128, 20
+    B = np.array([20, 3, 0, 11], np.int32)
+    T = int(B.sum())
+    idx = _random_routing(T, E, K, rng)
+    x = oracle.bf16_from_f32(rng.standard_normal((T, H)).astype(np.float32))
+    ll = oracle.dispatch_ll(x, idx, B, E, C)
+    eo = np.arange(E + 1, dtype=np.int32) * (R * C)            # expert e owns rows [e*R*C, (e+1)*R*C)
+    y = oracle.expert_scale(ll["recv"], None, eo, E)
+    w = rng.random((T, K)).astype(np.float32)
+    gather = oracle.combine(y, ll["tok2row"], w, out="f32")
+    ret = oracle.combine_ll_push(y, ll["row2src"], ll["counts"], R, E, C, T, K)
+    pushed = oracle.combine(ret, np.arange(T * K, dtype=np.int32), w, out="f32")
+    assert np.array_equal(gather.view(np.uint32), pushed.view(np.uint32))
+    # and both equal the throughput layout's combine
+    rg = oracle.dispatch(x, idx, B, E)
+    yr = oracle.expert_scale(rg["recv"], None, rg["expert_offsets"], E)
+    assert np.array_equal(oracle.combine(yr, rg["tok2row"], w, out="f32").view(np.uint32), gather.view(np.uint32))
