@@ -203,6 +203,57 @@ def time_call(fn, stream, reps: int = 50) -> float:
     return a.elapsed_time(z) * 1e3 / reps
 
 
+def time_flushed(fn, stream, flush, reps: int = 50) -> float:
+    """Mean µs of fn() with the L2 flushed (outside the events) before every call."""
+    for _ in range(3):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a, z in ev:
+        flush.fill_(3)
+        a.record(stream)
+        fn()
+        z.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(z) for a, z in ev) * 1e3
+
+
+def measure_decode_layouts(dev, stream, flush):
+    """DeepSeek-V3 decode layer (R=8, E=256, K=8, H=7168, 128 tokens/rank, bf16): dispatch and
+    combine through the throughput (ragged) layout and through the low-latency rectangle
+    (chunk cap C = 128), each call timed on its own with the L2 flushed."""
+    from combine_moe_route_gb300 import binding as b
+    from combine_moe_route_gb300 import workloads as wl
+    w = wl.WORKLOADS["dsv3_decode"]
+    inp = wl.generate(w, seed=0)
+    B, T, E, K, H, C = inp["B"], inp["T"], w.E, w.K, w.H, int(inp["B"].max())
+    R = w.R
+    x = inp["x"].to(dev)
+    idx, wts = b.route_topk(torch.from_numpy(inp["logits"]).to(dev), K)
+    d = b.dispatch(x, idx, B, E)
+    y = b.expert_scale(d.recv_x, None, d.expert_offsets, E)
+    out = b.combine(y, d.tok2row, wts)
+    dl = b.dispatch_ll(x, idx, B, E, C)
+    eo = torch.arange(E + 1, dtype=torch.int32, device=dev) * (R * C)
+    yl = b.expert_scale(dl.recv_x, None, eo, E)
+    outl = b.combine_ll(yl, E, R, C, dl.tok2row, wts)
+    ret = b.combine_ll_push(yl, dl, R, E, T, K)
+    torch.cuda.synchronize()
+    res = {
+        "ragged_dispatch_us": time_flushed(lambda: b.dispatch(x, idx, B, E, out=d), stream, flush),
+        "ragged_combine_us": time_flushed(lambda: b.combine(y, d.tok2row, wts, out=out), stream, flush),
+        "ll_dispatch_us": time_flushed(lambda: b.dispatch_ll(x, idx, B, E, C, out=dl), stream, flush),
+        "ll_combine_gather_us": time_flushed(lambda: b.combine_ll(yl, E, R, C, dl.tok2row, wts, out=outl),
+                                             stream, flush),
+        "ll_combine_push_us": time_flushed(lambda: b.combine_ll_push(yl, dl, R, E, T, K, out=ret), stream, flush),
+        "ll_combine_reduce_us": time_flushed(lambda: b.combine(ret, None, wts, out=outl), stream, flush),
+    }
+    db = dispatch_bytes(T, E, R, K, H, False)
+    cb = combine_bytes(T, K, H)
+    res["floor_us_at_8TBs"] = {"dispatch": db / 8e6, "combine": cb / 8e6}
+    return {"dsv3_decode_layouts": {k: (round(v, 2) if isinstance(v, float) else v) for k, v in res.items()}}
+
+
 def replica_value(per_rank_us: float, world: int) -> float:
     """Whole-job µs per layer for N independent replicas: the slowest rank's
     time per layer divided by the N layers processed in that time."""
@@ -429,6 +480,8 @@ def run_ours(args, world, rank, local):
 
         us = time_call(grouped, stream, reps=50)
         next_rows["route_grouped_G8_M4"] = {"us": us, "GBps": route_bytes(T, E, K) / (us * 1e-6) / 1e9}
+
+    next_rows.update(measure_decode_layouts(dev, stream, flush))
 
     # correctness of what was timed: the last step's outputs equal the first layer's
     st, code = b.get_device_error(d.workspace)

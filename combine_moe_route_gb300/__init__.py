@@ -14,7 +14,7 @@ _API = {
     "route_topk", "dispatch", "combine", "expert_scale", "dispatch_workspace_bytes",
     "get_device_error", "abi_version", "strerror", "MoeError", "DispatchResult",
     "moe_layer", "library_path", "load_library", "MOE_OK", "dispatch_noalloc",
-    "route_topk_grouped",
+    "route_topk_grouped", "dispatch_ll", "combine_ll", "combine_ll_push", "DispatchLLResult",
 }
 
 __all__ = sorted(_API) + ["workloads"]

@@ -68,6 +68,12 @@ def load_library() -> ctypes.CDLL:
         lib.moe_expert_scale.restype = i32
         lib.moe_combine.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
         lib.moe_combine.restype = i32
+        lib.moe_dispatch_ll.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.moe_dispatch_ll.restype = i32
+        lib.moe_combine_ll.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, i32, i32, vp, vp]
+        lib.moe_combine_ll.restype = i32
+        lib.moe_combine_ll_push.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        lib.moe_combine_ll_push.restype = i32
         lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
         lib.moe_get_device_error.restype = i32
         _lib = lib
@@ -279,9 +285,10 @@ def combine(y: torch.Tensor, tok2row: torch.Tensor, topk_w: torch.Tensor, *,
         raise ValueError("topk_w must be [T, K]")
     T, K = topk_w.shape
     H = y.shape[1]
-    _dev(tok2row, "tok2row", torch.int32)
-    if tok2row.numel() != T * K:
-        raise ValueError("tok2row must have T*K entries")
+    if tok2row is not None:       # None: the identity map (rows g*K + j)
+        _dev(tok2row, "tok2row", torch.int32)
+        if tok2row.numel() != T * K:
+            raise ValueError("tok2row must have T*K entries")
     if out_dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("out_dtype must be bfloat16 or float32")
     if out is None:
@@ -292,6 +299,86 @@ def combine(y: torch.Tensor, tok2row: torch.Tensor, topk_w: torch.Tensor, *,
             _ptr(y), _ptr(tok2row), _ptr(topk_w), T, K, H,
             _DTYPE_FP32 if out_dtype == torch.float32 else _DTYPE_BF16, _ptr(out),
             _stream_handle(stream, y.device)), "moe_combine")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# low-latency (fixed-rectangle) layout
+# ---------------------------------------------------------------------------
+
+@dataclass
+class DispatchLLResult:
+    recv_x: torch.Tensor             # [E*R*C, H] bf16 or float8_e4m3fn
+    recv_scale: torch.Tensor | None  # [E*R*C, H/128] fp32 (FP8 only)
+    counts: torch.Tensor             # [E*R] int32: filled rows per (expert, source rank) region
+    tok2row: torch.Tensor            # [T*K] int32
+    row2src: torch.Tensor            # [E*R*C] int32 (meaningful on filled rows only)
+    workspace: torch.Tensor
+    C: int
+
+
+def dispatch_ll(x: torch.Tensor, topk_idx: torch.Tensor, B, E: int, C: int, *, fp8: bool = False,
+                out: DispatchLLResult | None = None, stream=None) -> DispatchLLResult:
+    """Low-latency dispatch into a fixed [E*R*C, H] rectangle (C rows per (expert, rank) region)."""
+    _dev(x, "x", torch.bfloat16)
+    T, H = x.shape
+    _dev(topk_idx, "topk_idx", torch.int32)
+    K = topk_idx.shape[1]
+    Bh = _host_B(B)
+    R = Bh.size
+    if int(Bh.astype(np.int64).sum()) != T:
+        raise ValueError(f"sum(B) = {int(Bh.sum())} does not match x.shape[0] = {T}")
+    dev = x.device
+    rows = E * R * C
+    if out is None:
+        out = DispatchLLResult(
+            recv_x=torch.empty((rows, H), dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16, device=dev),
+            recv_scale=torch.empty((rows, H // 128), dtype=torch.float32, device=dev) if fp8 else None,
+            counts=torch.empty(E * R, dtype=torch.int32, device=dev),
+            tok2row=torch.empty(T * K, dtype=torch.int32, device=dev),
+            row2src=torch.empty(rows, dtype=torch.int32, device=dev),
+            workspace=torch.empty(max(dispatch_workspace_bytes(R, E, K, T), 256), dtype=torch.uint8, device=dev),
+            C=C)
+    with torch.cuda.device(dev):
+        _check(load_library().moe_dispatch_ll(
+            _ptr(x), _ptr(topk_idx), R, Bh.ctypes.data, E, K, H, C, _DTYPE_FP8 if fp8 else _DTYPE_BF16,
+            _ptr(out.recv_x), _ptr(out.recv_scale) if fp8 else None, _ptr(out.counts), _ptr(out.tok2row),
+            _ptr(out.row2src), _ptr(out.workspace), out.workspace.numel(), _stream_handle(stream, dev)),
+            "moe_dispatch_ll")
+    return out
+
+
+def combine_ll(y: torch.Tensor, E: int, R: int, C: int, tok2row: torch.Tensor, topk_w: torch.Tensor, *,
+               out_dtype: torch.dtype = torch.bfloat16, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Weighted sum gathered from the low-latency rectangle y [E*R*C, H]."""
+    _dev(y, "y", torch.bfloat16)
+    _dev(tok2row, "tok2row", torch.int32)
+    _dev(topk_w, "topk_w", torch.float32)
+    T, K = topk_w.shape
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=y.device)
+    _dev(out, "out", out_dtype, (T, H))
+    with torch.cuda.device(y.device):
+        _check(load_library().moe_combine_ll(
+            _ptr(y), E, R, C, _ptr(tok2row), _ptr(topk_w), T, K, H,
+            _DTYPE_FP32 if out_dtype == torch.float32 else _DTYPE_BF16, _ptr(out), _stream_handle(stream, y.device)),
+            "moe_combine_ll")
+    return out
+
+
+def combine_ll_push(y: torch.Tensor, d: DispatchLLResult, R: int, E: int, T: int, K: int, *,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Push each filled rectangle row to its origin slot g*K + j: ret [T*K, H] bf16."""
+    _dev(y, "y", torch.bfloat16)
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty((T * K, H), dtype=torch.bfloat16, device=y.device)
+    _dev(out, "ret", torch.bfloat16, (T * K, H))
+    with torch.cuda.device(y.device):
+        _check(load_library().moe_combine_ll_push(
+            _ptr(y), _ptr(d.row2src), _ptr(d.counts), R, E, d.C, K, H, T, _ptr(out),
+            _stream_handle(stream, y.device)), "moe_combine_ll_push")
     return out
 
 

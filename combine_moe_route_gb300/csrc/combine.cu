@@ -28,21 +28,22 @@ namespace moe {
 constexpr int kCombineThreads = 128;
 constexpr int kCombineBatch = 8;   // row loads in flight per chunk
 
+// tok2row == nullptr reads row g*K + j (the layout a push-style return leaves
+// on the origin rank); rows = number of rows of y (indices outside are skipped).
 template <bool kOutF32>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __nv_bfloat16 *__restrict__ y,
                                                                   const int32_t *__restrict__ tok2row,
                                                                   const float *__restrict__ topk_w, int T, int K,
-                                                                  int H, void *__restrict__ out) {
+                                                                  int H, long long rows, void *__restrict__ out) {
     __shared__ int32_t s_row[MOE_MAX_TOPK];
     __shared__ float s_w[MOE_MAX_TOPK];
-    const long long rows = (long long)T * K;
     const int nchunk = H / 8;
 
     for (long long g = blockIdx.x; g < T; g += gridDim.x) {
         __syncthreads();   // previous token's readers are done with s_row / s_w
         if (threadIdx.x < K) {
-            const int r = __ldg(tok2row + g * K + threadIdx.x);
-            s_row[threadIdx.x] = (r >= 0 && r < rows) ? r : -1;
+            const long long r = tok2row ? (long long)__ldg(tok2row + g * K + threadIdx.x) : g * K + threadIdx.x;
+            s_row[threadIdx.x] = (r >= 0 && r < rows) ? (int32_t)r : -1;
             s_w[threadIdx.x] = __ldg(topk_w + g * K + threadIdx.x);
         }
         __syncthreads();
@@ -92,15 +93,60 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __nv_bfl
 }
 
 cudaError_t launch_combine(const void *y, const int32_t *tok2row, const float *topk_w, int T, int K, int H,
-                           bool out_f32, void *out, cudaStream_t stream) {
+                           bool out_f32, void *out, long long rows, cudaStream_t stream) {
     long long grid = (long long)device_sm_count() * 16;
     if (grid > T) grid = T;
     if (grid < 1) grid = 1;
     const __nv_bfloat16 *yb = static_cast<const __nv_bfloat16 *>(y);
     if (out_f32)
-        combine_kernel<true><<<(unsigned)grid, kCombineThreads, 0, stream>>>(yb, tok2row, topk_w, T, K, H, out);
+        combine_kernel<true><<<(unsigned)grid, kCombineThreads, 0, stream>>>(yb, tok2row, topk_w, T, K, H, rows, out);
     else
-        combine_kernel<false><<<(unsigned)grid, kCombineThreads, 0, stream>>>(yb, tok2row, topk_w, T, K, H, out);
+        combine_kernel<false><<<(unsigned)grid, kCombineThreads, 0, stream>>>(yb, tok2row, topk_w, T, K, H, rows, out);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------------------
+// push-style return of the low-latency layout
+// --------------------------------------------------------------------------
+// lehuy.net, "Decoding high-performance EP kernels", "Optimising for latency":
+// dispatch tagged each token with its origin, so the expert's host writes each
+// output straight to a private slot on the origin rank indexed by the token's
+// position there and by which of its K experts produced it.  Here: blocks walk
+// the (expert, source rank) regions; a block reads the region's count once and
+// its warps copy the filled rows, 16 bytes per lane, to ret[row2src[row]].
+constexpr int kPushThreads = 128;
+
+__global__ void __launch_bounds__(kPushThreads) combine_push_kernel(const __nv_bfloat16 *__restrict__ y,
+                                                                    const int32_t *__restrict__ row2src,
+                                                                    const int32_t *__restrict__ counts, int C, int H,
+                                                                    long long regions, long long ret_rows,
+                                                                    __nv_bfloat16 *__restrict__ ret) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    for (long long region = blockIdx.x; region < regions; region += gridDim.x) {
+        const int n = min(__ldg(counts + region), C);
+        for (int slot = warp; slot < n; slot += nwarps) {
+            const long long r = region * C + slot;
+            const long long dst = __ldg(row2src + r);
+            if (dst < 0 || dst >= ret_rows) continue;
+            const __nv_bfloat16 *src = y + r * H;
+            __nv_bfloat16 *d = ret + dst * H;
+            for (int c = lane; c < H / 8; c += 32) st_v4(d + (size_t)c * 8, ld_stream_v4(src + (size_t)c * 8));
+        }
+    }
+}
+
+cudaError_t launch_combine_push(const void *y, const int32_t *row2src, const int32_t *counts, int C, int H,
+                                long long rect_rows, long long ret_rows, void *ret, cudaStream_t stream) {
+    const long long regions = rect_rows / C;
+    long long grid = regions;
+    const long long cap = (long long)device_sm_count() * 16;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    combine_push_kernel<<<(unsigned)grid, kPushThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(y), row2src,
+                                                                     counts, C, H, regions, ret_rows,
+                                                                     static_cast<__nv_bfloat16 *>(ret));
     return cudaGetLastError();
 }
 

@@ -256,7 +256,9 @@ struct ScatterArgs {
     int32_t *tok2row;          // in: in-tile ranks; out: rows
     int32_t *row2src;
     int32_t *err;
+    const int32_t *tile_hist;  // [E * ntiles] (low-latency layout)
     int T, E, K, H;
+    int C;                     // low-latency layout: rows per (expert, source rank) region
     int stages;
 };
 
@@ -311,7 +313,11 @@ __host__ __device__ inline size_t scatter_stage_bytes(int H, bool fp8) {
 //      stores of the scale row; otherwise the lanes store the scales);
 //   5. once the previous token's stores have read their stage, lane 0 refills
 //      that stage with the token S - 1 ahead.
-template <bool kFp8>
+//
+// kLL (low-latency layout): the destination is a fixed rectangle with C rows
+// per (expert, source rank) region; row = (e*R + s)*C + (tokens of rank s
+// routed to e in the rank's earlier tiles) + in-tile rank.  No scan is needed.
+template <bool kFp8, bool kLL>
 __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const ScatterArgs a,
                                                                          const __grid_constant__ RankTable rt) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -357,8 +363,18 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
     __syncwarp();
     pdl_wait();
 
-    // counts / offsets / expert_offsets from the scanned histogram
-    {
+    if (kLL) {
+        // counts[e*R + s]: the rank's tile totals for expert e
+        const int n = E * rt.R;
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+            const int e = i / rt.R;
+            const int s = i - e * rt.R;
+            int c = 0;
+            for (int tau = rt.tile_off[s]; tau < rt.tile_off[s + 1]; ++tau) c += a.tile_hist[(long long)e * rt.ntiles + tau];
+            a.counts[i] = c;
+        }
+    } else {
+        // counts / offsets / expert_offsets from the scanned histogram
         const int n = E * rt.R;
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= n; i += gridDim.x * blockDim.x) {
             if (i < n) {
@@ -394,7 +410,14 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
                 const int lr = a.tok2row[i];
                 if (e >= 0 && e < E && lr >= 0) {
                     const int tile = rt.tile_off[sidx] + (int)((i - item0) / kTileItems);
-                    row = a.scan[(long long)e * rt.ntiles + tile] + lr;
+                    if (kLL) {
+                        int base = (e * rt.R + sidx) * a.C;
+                        for (int tau = rt.tile_off[sidx]; tau < tile; ++tau)
+                            base += a.tile_hist[(long long)e * rt.ntiles + tau];
+                        row = base + lr;
+                    } else {
+                        row = a.scan[(long long)e * rt.ntiles + tile] + lr;
+                    }
                     a.row2src[row] = (int32_t)i;
                 } else {
                     e = -1;
@@ -518,6 +541,48 @@ static int sm_count() {
 
 int device_sm_count() { return sm_count(); }
 
+// Persistent launch of the scatter (one wave), with programmatic stream
+// serialization so that it stages its first rows while the previous kernel ends.
+static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, bool ll, cudaStream_t stream) {
+    const long long T = a.T;
+    const int H = a.H;
+    cudaError_t ce;
+    const size_t smem = scatter_stage_bytes(H, fp8) * MOE_SCATTER_STAGES * MOE_SCATTER_WARPS;
+    a.stages = MOE_SCATTER_STAGES;
+    const void *kfn = fp8 ? (ll ? (const void *)scatter_kernel<true, true> : (const void *)scatter_kernel<true, false>)
+                          : (ll ? (const void *)scatter_kernel<false, true> : (const void *)scatter_kernel<false, false>);
+    if ((ce = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return ce;
+    int per_sm = 0;
+    if ((ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, MOE_SCATTER_WARPS * 32, smem)) !=
+        cudaSuccess)
+        return ce;
+    if (per_sm < 1) per_sm = 1;
+    long long grid = (long long)sm_count() * per_sm;   // persistent: one wave
+    const long long need = (T + MOE_SCATTER_WARPS - 1) / MOE_SCATTER_WARPS;
+    if (grid > need) grid = need;
+    if (grid < 1) grid = 1;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(MOE_SCATTER_WARPS * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (fp8)
+        ce = ll ? cudaLaunchKernelEx(&cfg, scatter_kernel<true, true>, a, rt)
+                : cudaLaunchKernelEx(&cfg, scatter_kernel<true, false>, a, rt);
+    else
+        ce = ll ? cudaLaunchKernelEx(&cfg, scatter_kernel<false, true>, a, rt)
+                : cudaLaunchKernelEx(&cfg, scatter_kernel<false, false>, a, rt);
+    if (ce != cudaSuccess) return ce;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
                             bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *offsets,
                             int32_t *expert_offsets, int32_t *tok2row, int32_t *row2src, void *workspace,
@@ -554,7 +619,7 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
             return ce;
     }
 
-    ScatterArgs a;
+    ScatterArgs a{};
     a.x = static_cast<const __nv_bfloat16 *>(x);
     a.topk_idx = topk_idx;
     a.scan = scan;
@@ -570,38 +635,41 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
     a.E = E;
     a.K = K;
     a.H = H;
-
-    const size_t smem = scatter_stage_bytes(H, fp8) * MOE_SCATTER_STAGES * MOE_SCATTER_WARPS;
-    a.stages = MOE_SCATTER_STAGES;
-    const void *kfn = fp8 ? (const void *)scatter_kernel<true> : (const void *)scatter_kernel<false>;
-    if ((ce = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-        return ce;
-    int per_sm = 0;
-    if ((ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, MOE_SCATTER_WARPS * 32, smem)) !=
-        cudaSuccess)
-        return ce;
-    if (per_sm < 1) per_sm = 1;
-    long long grid = (long long)sm_count() * per_sm;              // persistent: one wave
-    const long long need = (T + MOE_SCATTER_WARPS - 1) / MOE_SCATTER_WARPS;
-    if (grid > need) grid = need;
-    if (grid < 1) grid = 1;
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(MOE_SCATTER_WARPS * 32);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (fp8)
-        ce = cudaLaunchKernelEx(&cfg, scatter_kernel<true>, a, rt);
-    else
-        ce = cudaLaunchKernelEx(&cfg, scatter_kernel<false>, a, rt);
-    if (ce != cudaSuccess) return ce;
-    return cudaGetLastError();
+    return launch_scatter(a, rt, fp8, false, stream);
 }
+
+cudaError_t launch_dispatch_ll(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
+                               int C, bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *tok2row,
+                               int32_t *row2src, void *workspace, cudaStream_t stream) {
+    const long long T = rt.rank_off[rt.R];
+    const DispatchPlan p = plan_dispatch(E, rt.ntiles);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    int32_t *err = reinterpret_cast<int32_t *>(ws);
+    int32_t *tile_hist = reinterpret_cast<int32_t *>(ws + p.off_hist);
+
+    cudaError_t ce = cudaMemsetAsync(ws, 0, kWsHeader, stream);   // error word
+    if (ce != cudaSuccess) return ce;
+    const size_t hist_smem = (size_t)kHistWarps * E * 4;
+    tile_hist_kernel<<<rt.ntiles, kHistThreads, hist_smem, stream>>>(topk_idx, E, K, rt, tile_hist, tok2row, err);
+    if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
+
+    ScatterArgs a{};
+    a.x = static_cast<const __nv_bfloat16 *>(x);
+    a.topk_idx = topk_idx;
+    a.recv_x = recv_x;
+    a.recv_scale = recv_scale;
+    a.counts = counts;
+    a.tok2row = tok2row;
+    a.row2src = row2src;
+    a.err = err;
+    a.tile_hist = tile_hist;
+    a.T = (int)T;
+    a.E = E;
+    a.K = K;
+    a.H = H;
+    a.C = C;
+    return launch_scatter(a, rt, fp8, true, stream);
+}
+
 
 }  // namespace moe

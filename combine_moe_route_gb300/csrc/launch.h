@@ -28,8 +28,13 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
                             bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *offsets,
                             int32_t *expert_offsets, int32_t *tok2row, int32_t *row2src, void *workspace,
                             cudaStream_t stream);
+cudaError_t launch_dispatch_ll(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
+                               int C, bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *tok2row,
+                               int32_t *row2src, void *workspace, cudaStream_t stream);
 cudaError_t launch_combine(const void *y, const int32_t *tok2row, const float *topk_w, int T, int K, int H,
-                           bool out_f32, void *out, cudaStream_t stream);
+                           bool out_f32, void *out, long long rows, cudaStream_t stream);
+cudaError_t launch_combine_push(const void *y, const int32_t *row2src, const int32_t *counts, int C, int H,
+                                long long rect_rows, long long ret_rows, void *ret, cudaStream_t stream);
 cudaError_t launch_expert_scale(const void *recv, const float *recv_scale, bool fp8, const int32_t *expert_offsets,
                                 int E, int H, int rows, int identity, void *y, cudaStream_t stream);
 

@@ -261,7 +261,8 @@ MOE_API moe_status moe_expert_scale(const void *recv_x, const float *recv_scale,
  *   y          device bf16 [T*K, H], 16-byte aligned: expert outputs in the
  *              dispatch row order.
  *   tok2row    device int32 [T*K]: from moe_dispatch.  Entries outside
- *              [0, T*K) contribute nothing.
+ *              [0, T*K) contribute nothing.  NULL means the identity map
+ *              (row g*K + j), the layout moe_combine_ll_push leaves.
  *   topk_w     device fp32 [T, K]: routing weights.
  *   out_dtype  MOE_DTYPE_BF16 or MOE_DTYPE_FP32.
  *   out        device [T, H] of out_dtype, 16-byte aligned:
@@ -274,6 +275,64 @@ MOE_API moe_status moe_expert_scale(const void *recv_x, const float *recv_scale,
 MOE_API moe_status moe_combine(const void *y, const int32_t *tok2row, const float *topk_w,
                        int T, int K, int H, moe_dtype out_dtype, void *out,
                        moe_stream_t stream);
+
+/*
+ * moe_dispatch_ll -- the low-latency dispatch ([EPK] "Optimising for latency:
+ * send without asking"): instead of a packed buffer whose layout needs a
+ * prefix sum over the real counts, every (source rank, expert) pair owns a
+ * fixed region of C rows, sized for the worst case, so the destination of a
+ * token is a static formula and the scan disappears from the path; C is the
+ * cap on the tokens a rank dispatches per call.  Copy j of token g (rank s,
+ * expert e) goes to row (e*R + s)*C + slot, slot = the number of rank s's
+ * earlier tokens routed to e (the same order as moe_dispatch's).
+ *
+ *   x, topk_idx, R, B, E, K, H, recv_dtype, workspace: as moe_dispatch (the
+ *              workspace size moe_dispatch_workspace_bytes(R, E, K, T) is
+ *              enough); every B[s] <= C.
+ *   C          rows per region, >= 1, with E*R*C < 2^31.
+ *   recv_x     device [E*R*C, H] of recv_dtype: out.  Rows at or past
+ *              counts[e*R + s] in a region are not written.
+ *   recv_scale device fp32 [E*R*C, H/128]: out, FP8 only.
+ *   counts     device int32 [E*R]: out, filled rows of region (e, s).
+ *   tok2row    device int32 [T*K]: out, row of copy j of token g.
+ *   row2src    device int32 [E*R*C]: out, g*K + j for each filled row; other
+ *              rows are not written.
+ * Errors: as moe_dispatch; MOE_ERR_INVALID_ARG also for C < 1, B[s] > C or
+ * E*R*C >= 2^31.  T == 0 writes zeros to counts and launches no kernel.
+ */
+MOE_API moe_status moe_dispatch_ll(const void *x, const int32_t *topk_idx, int R, const int32_t *B,
+                                   int E, int K, int H, int C, moe_dtype recv_dtype,
+                                   void *recv_x, float *recv_scale, int32_t *counts,
+                                   int32_t *tok2row, int32_t *row2src,
+                                   void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_combine_ll -- moe_combine over the low-latency rectangle: y is
+ * [E*R*C, H] bf16 (expert outputs in moe_dispatch_ll's rows), tok2row is
+ * moe_dispatch_ll's; indices outside [0, E*R*C) contribute nothing.  The sum,
+ * its order and rounding, and the errors are those of moe_combine.
+ */
+MOE_API moe_status moe_combine_ll(const void *y, int E, int R, int C, const int32_t *tok2row,
+                                  const float *topk_w, int T, int K, int H, moe_dtype out_dtype,
+                                  void *out, moe_stream_t stream);
+
+/*
+ * moe_combine_ll_push -- the push-style return of the low-latency layout
+ * ([EPK] "Optimising for latency": the expert's host writes each output
+ * straight to a private slot on the token's origin rank, indexed by the
+ * token's position there and by which of its K experts produced it).  For
+ * every filled row of the rectangle (slot < counts[region]),
+ * ret[row2src[row]] = y[row].  moe_combine with tok2row = NULL then forms
+ * the weighted sums on the origin side.
+ *
+ *   y        device bf16 [E*R*C, H], 16-byte aligned.
+ *   row2src, counts  from moe_dispatch_ll.
+ *   ret      device bf16 [T*K, H], 16-byte aligned: out.
+ * Errors: MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_CUDA.
+ */
+MOE_API moe_status moe_combine_ll_push(const void *y, const int32_t *row2src, const int32_t *counts,
+                                       int R, int E, int C, int K, int H, int T, void *ret,
+                                       moe_stream_t stream);
 
 /*
  * moe_get_device_error -- SYNCHRONOUS: waits for `stream`, then copies the
