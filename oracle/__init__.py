@@ -86,6 +86,9 @@ def _load():
                 _vp, _f32p, ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16p]
             lib.oracle_combine.argtypes = [
                 _u16p, _i32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _u16p, _f32p]
+            lib.oracle_combine_partial.argtypes = [
+                _u16p, _i32p, _i32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                _u16p, _u16p, _f32p]
             lib.oracle_combine_f64.argtypes = [
                 _u16p, _i32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64p]
             _lib = lib
@@ -294,6 +297,27 @@ def combine(y_bf16: np.ndarray, tok2row: np.ndarray, topk_w: np.ndarray, out: st
         lib.oracle_combine(_ptr(y, _u16p), _ptr(t2r, _i32p), _ptr(w, _f32p), T, K, H, _ptr(o, _u16p), None)
         return o
     raise ValueError(out)
+
+
+def combine_partial(y_bf16: np.ndarray, tok2row: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray,
+                    E: int, R: int, out: str = "bf16", with_partial: bool = False):
+    """Sender-side partial accumulation: bf16 partial per (token, expert rank), summed on the origin.
+
+    Returns out (bf16 bits or fp32), and with ``with_partial`` also the [T*K, H] partial rows
+    (bf16 bits; only slot g*K + j0 of each (token, rank) is meaningful, the rest stays 0)."""
+    y = _c(y_bf16, np.uint16)
+    t2r = _c(tok2row, np.int32).reshape(-1)
+    idx = _c(topk_idx, np.int32)
+    w = _c(topk_w, np.float32)
+    T, K = w.shape
+    H = y.shape[1]
+    part = np.zeros((T * K, H), np.uint16) if with_partial else None
+    ob = np.empty((T, H), np.uint16) if out == "bf16" else None
+    of = np.empty((T, H), np.float32) if out == "f32" else None
+    _load().oracle_combine_partial(_ptr(y, _u16p), _ptr(t2r, _i32p), _ptr(idx.reshape(-1), _i32p), _ptr(w, _f32p),
+                                   T, K, H, E, R, _ptr(part, _u16p), _ptr(ob, _u16p), _ptr(of, _f32p))
+    o = ob if out == "bf16" else of
+    return (o, part) if with_partial else o
 
 
 def layer(x_bf16, logits, B, E: int, K: int, fp8: bool = False, identity: bool = False,

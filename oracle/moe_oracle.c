@@ -37,6 +37,7 @@
  *   oracle_dispatch_ll / oracle_combine_ll_push   pinned (same slots and payload as the ragged layout)
  *   oracle_expert_scale                           pinned (library arithmetic)
  *   oracle_combine / oracle_combine_f64           pinned (identity experts, one-hot, error bound)
+ *   oracle_combine_partial                        pinned (R = 1 gives the receive-side result, slots, bound)
  */
 #include <math.h>
 #include <stdint.h>
@@ -449,6 +450,45 @@ void oracle_combine(const uint16_t *y, const int32_t *tok2row, const float *topk
                 int32_t row = tok2row[g * K + j];
                 float v = oracle_f32_from_bf16(y[(int64_t)row * H + h]);
                 acc = fmaf(topk_w[g * K + j], v, acc);
+            }
+            if (out_f32) out_f32[g * H + h] = acc;
+            if (out_bf16) out_bf16[g * H + h] = oracle_bf16_from_f32(acc);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sender-side partial accumulation: [EFA] "Evaluation" (DeepEP accumulates  */
+/* on the sending side of combine to cut the bytes returned; doing so may    */
+/* affect precision; pplx accumulates on the receiving side).  Reading (no   */
+/* formula on the page): rank r hosts the experts e with e / (E/R) == r; for */
+/* each token g and each rank r hosting at least one of g's experts,         */
+/*   p[g,r] = bf16( fp32 fma chain over those copies j, ascending j, from +0 ) */
+/* is the one row returned, stored in slot g*K + j0 with j0 the first such j. */
+/* The origin then adds its partials in ascending r, in fp32 from +0, and     */
+/* rounds to bf16 (out_bf16) or keeps fp32 (out_f32).  `partial` may be NULL. */
+/* ------------------------------------------------------------------------ */
+void oracle_combine_partial(const uint16_t *y, const int32_t *tok2row, const int32_t *topk_idx,
+                            const float *topk_w, int T, int K, int H, int E, int R,
+                            uint16_t *partial, uint16_t *out_bf16, float *out_f32)
+{
+    int L = E / R;
+    for (int64_t g = 0; g < T; ++g) {
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int r = 0; r < R; ++r) {
+                int j0 = -1;
+                float part = 0.0f;
+                for (int j = 0; j < K; ++j) {
+                    if (topk_idx[g * K + j] / L != r) continue;
+                    if (j0 < 0) j0 = j;
+                    int32_t row = tok2row[g * K + j];
+                    part = fmaf(topk_w[g * K + j], oracle_f32_from_bf16(y[(int64_t)row * H + h]), part);
+                }
+                if (j0 < 0) continue;                       /* no expert of g on rank r */
+                uint16_t wire = oracle_bf16_from_f32(part);  /* the row that would travel back */
+                if (partial) partial[(g * K + j0) * (int64_t)H + h] = wire;
+                acc = acc + oracle_f32_from_bf16(wire);
             }
             if (out_f32) out_f32[g * H + h] = acc;
             if (out_bf16) out_bf16[g * H + h] = oracle_bf16_from_f32(acc);

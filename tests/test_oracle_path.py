@@ -458,3 +458,54 @@ def test_ll_push_then_reduce_equals_gather(oracle):
     rg = oracle.dispatch(x, idx, B, E)
     yr = oracle.expert_scale(rg["recv"], None, rg["expert_offsets"], E)
     assert np.array_equal(oracle.combine(yr, rg["tok2row"], w, out="f32").view(np.uint32), gather.view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# sender-side partial accumulation
+# --------------------------------------------------------------------------
+
+def _partial_case(oracle, R, E, K, H, T, seed):
+    rng = np.random.default_rng(seed)
+    idx = _random_routing(T, E, K, rng)
+    y = oracle.bf16_from_f32(rng.standard_normal((T * K, H)).astype(np.float32))
+    t2r = rng.permutation(T * K).astype(np.int32)
+    w = rng.random((T, K)).astype(np.float32)
+    w /= w.sum(1, keepdims=True)
+    return idx, y, t2r, w
+
+
+def test_partial_with_one_rank_is_receive_side(oracle):
+    # all experts on one rank: the single partial is the receive-side fp32 sum, rounded once
+    idx, y, t2r, w = _partial_case(oracle, 1, 16, 4, 64, 40, 40)
+    assert np.array_equal(oracle.combine_partial(y, t2r, idx, w, 16, 1), oracle.combine(y, t2r, w))
+    f = oracle.combine_partial(y, t2r, idx, w, 16, 1, out="f32")
+    assert np.array_equal(f, oracle.f32_from_bf16(oracle.combine(y, t2r, w)))
+
+
+def test_partial_slots_and_error_bound(oracle):
+    R, E, K, H, T = 8, 64, 8, 128, 60
+    idx, y, t2r, w = _partial_case(oracle, R, E, K, H, T, 41)
+    out, part = oracle.combine_partial(y, t2r, idx, w, E, R, out="f32", with_partial=True)
+    L = E // R
+    yf = oracle.f32_from_bf16(y).astype(np.float64)
+    exact = np.zeros((T, H))
+    bound = np.zeros((T, H))
+    for g in range(T):
+        ranks = idx[g] // L
+        for r in np.unique(ranks):                            # numpy's own grouping of the K copies
+            js = np.nonzero(ranks == r)[0]
+            s = sum(float(w[g, j]) * yf[t2r[g * K + j]] for j in js)
+            exact[g] += s
+            # the partial travels in slot g*K + (first j of the rank)
+            pr = oracle.f32_from_bf16(part[g * K + js[0]]).astype(np.float64)
+            mag = sum(abs(float(w[g, j])) * np.abs(yf[t2r[g * K + j]]) for j in js)
+            assert np.all(np.abs(pr - s) <= np.abs(s) * 2.0**-8 + mag * len(js) * 2.0**-23 + 1e-30)
+            bound += np.abs(s) * 2.0**-8 + mag * len(js) * 2.0**-23
+        # slots of non-first copies are not written
+        firsts = {int(np.nonzero(ranks == r)[0][0]) for r in np.unique(ranks)}
+        for j in range(K):
+            if j not in firsts:
+                assert np.all(part[g * K + j] == 0)
+    n_ranks_max = K
+    bound += np.abs(exact) * n_ranks_max * 2.0**-23
+    assert np.all(np.abs(out - exact) <= bound + 1e-30)
