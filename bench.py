@@ -254,6 +254,38 @@ def measure_decode_layouts(dev, stream, flush):
     return {"dsv3_decode_layouts": {k: (round(v, 2) if isinstance(v, float) else v) for k, v in res.items()}}
 
 
+def measure_partial_combine(b, y, d, idx, wts, out, E, R, K, H, T, stream, flush):
+    """Sender-side partial accumulation on the benchmark layer: time of the send and receive
+    halves, rows that would travel back (one per (token, expert rank) instead of one per copy),
+    and the error of both combine forms against an fp64 sum on 256 sampled tokens."""
+    part = b.combine_partial_send(y, d.tok2row, idx, wts, E, R)
+    op = b.combine_partial_recv(part, idx, E, R)
+    torch.cuda.synchronize()
+    send_us = time_flushed(lambda: b.combine_partial_send(y, d.tok2row, idx, wts, E, R, out=part), stream, flush)
+    recv_us = time_flushed(lambda: b.combine_partial_recv(part, idx, E, R, out=op), stream, flush)
+    ranks = (idx // (E // R)).cpu().numpy()
+    distinct = int(sum(len(np.unique(r)) for r in ranks))
+    # precision on a sample of tokens: both forms against an fp64 sum of the same bf16 inputs
+    rng = np.random.default_rng(0)
+    g = np.sort(rng.choice(T, size=min(256, T), replace=False))
+    rows = d.tok2row.view(T, K)[torch.from_numpy(g).to(y.device)].reshape(-1).long()
+    yv = y.index_select(0, rows).float().cpu().numpy().astype(np.float64).reshape(len(g), K, H)
+    wv = wts.cpu().numpy()[g].astype(np.float64)
+    exact = np.einsum("tk,tkh->th", wv, yv)
+    errs = {}
+    for name, o in (("receive_side", out), ("sender_side", op)):
+        ov = o.float().cpu().numpy()[g].astype(np.float64)
+        err = np.abs(ov - exact)
+        ulp = np.maximum(np.abs(exact), 2.0**-126) * 2.0**-8
+        errs[name] = {"rms_rel": float(np.sqrt((err**2).mean() / (exact**2).mean())),
+                      "max_bf16_ulp": float((err / ulp).max())}
+    return {"partial_combine": {
+        "send_us": round(send_us, 2), "recv_us": round(recv_us, 2),
+        "rows_returned": distinct, "rows_returned_receive_side": T * K,
+        "return_bytes_saved_frac": round(1.0 - distinct / (T * K), 4),
+        "error_vs_fp64": errs}}
+
+
 def replica_value(per_rank_us: float, world: int) -> float:
     """Whole-job µs per layer for N independent replicas: the slowest rank's
     time per layer divided by the N layers processed in that time."""
@@ -482,6 +514,7 @@ def run_ours(args, world, rank, local):
         next_rows["route_grouped_G8_M4"] = {"us": us, "GBps": route_bytes(T, E, K) / (us * 1e-6) / 1e9}
 
     next_rows.update(measure_decode_layouts(dev, stream, flush))
+    next_rows.update(measure_partial_combine(b, y, d, idx, wts, out, E, w.R, K, H, T, stream, flush))
 
     # correctness of what was timed: the last step's outputs equal the first layer's
     st, code = b.get_device_error(d.workspace)

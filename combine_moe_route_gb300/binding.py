@@ -74,6 +74,10 @@ def load_library() -> ctypes.CDLL:
         lib.moe_combine_ll.restype = i32
         lib.moe_combine_ll_push.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
         lib.moe_combine_ll_push.restype = i32
+        lib.moe_combine_partial_send.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+        lib.moe_combine_partial_send.restype = i32
+        lib.moe_combine_partial_recv.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        lib.moe_combine_partial_recv.restype = i32
         lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
         lib.moe_get_device_error.restype = i32
         _lib = lib
@@ -379,6 +383,47 @@ def combine_ll_push(y: torch.Tensor, d: DispatchLLResult, R: int, E: int, T: int
         _check(load_library().moe_combine_ll_push(
             _ptr(y), _ptr(d.row2src), _ptr(d.counts), R, E, d.C, K, H, T, _ptr(out),
             _stream_handle(stream, y.device)), "moe_combine_ll_push")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# sender-side partial accumulation
+# ---------------------------------------------------------------------------
+
+def combine_partial_send(y: torch.Tensor, tok2row: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                         E: int, R: int, *, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One bf16 partial per (token, expert rank) in slot g*K + (first copy on that rank): [T*K, H]."""
+    _dev(y, "y", torch.bfloat16)
+    _dev(tok2row, "tok2row", torch.int32)
+    _dev(topk_idx, "topk_idx", torch.int32)
+    _dev(topk_w, "topk_w", torch.float32)
+    T, K = topk_w.shape
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty((T * K, H), dtype=torch.bfloat16, device=y.device)
+    _dev(out, "partial", torch.bfloat16, (T * K, H))
+    with torch.cuda.device(y.device):
+        _check(load_library().moe_combine_partial_send(
+            _ptr(y), _ptr(tok2row), _ptr(topk_idx), _ptr(topk_w), T, K, H, E, R, _ptr(out),
+            _stream_handle(stream, y.device)), "moe_combine_partial_send")
+    return out
+
+
+def combine_partial_recv(partial: torch.Tensor, topk_idx: torch.Tensor, E: int, R: int, *,
+                         out_dtype: torch.dtype = torch.bfloat16, out: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """Sum of each token's partials in ascending rank order (fp32) -> [T, H]."""
+    _dev(partial, "partial", torch.bfloat16)
+    _dev(topk_idx, "topk_idx", torch.int32)
+    T, K = topk_idx.shape
+    H = partial.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=partial.device)
+    _dev(out, "out", out_dtype, (T, H))
+    with torch.cuda.device(partial.device):
+        _check(load_library().moe_combine_partial_recv(
+            _ptr(partial), _ptr(topk_idx), T, K, H, E, R, _DTYPE_FP32 if out_dtype == torch.float32 else _DTYPE_BF16,
+            _ptr(out), _stream_handle(stream, partial.device)), "moe_combine_partial_recv")
     return out
 
 

@@ -196,6 +196,30 @@ moe_status moe_combine_ll_push(const void *y, const int32_t *row2src, const int3
                                                 (cudaStream_t)stream));
 }
 
+moe_status moe_combine_partial_send(const void *y, const int32_t *tok2row, const int32_t *topk_idx,
+                                    const float *topk_w, int T, int K, int H, int E, int R, void *partial,
+                                    moe_stream_t stream) {
+    if (T < 0 || R < 1 || R > MOE_MAX_RANKS || !topk_shape_ok(E, K) || E % R != 0) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0 || (long long)T * K >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y || !tok2row || !topk_idx || !topk_w || !partial) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(partial)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(
+        moe::launch_combine_partial(y, tok2row, topk_idx, topk_w, T, K, H, E, R, partial, (cudaStream_t)stream));
+}
+
+moe_status moe_combine_partial_recv(const void *partial, const int32_t *topk_idx, int T, int K, int H, int E, int R,
+                                    moe_dtype out_dtype, void *out, moe_stream_t stream) {
+    if (T < 0 || R < 1 || R > MOE_MAX_RANKS || !topk_shape_ok(E, K) || E % R != 0) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0 || (long long)T * K >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+    if (out_dtype != MOE_DTYPE_BF16 && out_dtype != MOE_DTYPE_FP32) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!partial || !topk_idx || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(partial) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(moe::launch_combine_partial_recv(partial, topk_idx, T, K, H, E, R, out_dtype == MOE_DTYPE_FP32,
+                                                        out, (cudaStream_t)stream));
+}
+
 moe_status moe_get_device_error(const void *workspace, int32_t *host_code, moe_stream_t stream) {
     if (!workspace || !host_code) return MOE_ERR_INVALID_ARG;
     int32_t v = 0;

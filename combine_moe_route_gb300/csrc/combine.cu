@@ -150,4 +150,197 @@ cudaError_t launch_combine_push(const void *y, const int32_t *row2src, const int
     return cudaGetLastError();
 }
 
+// --------------------------------------------------------------------------
+// sender-side partial accumulation
+// --------------------------------------------------------------------------
+// Perplexity, "Enabling trillion-parameter models on AWS EFA", "Evaluation":
+// DeepEP accumulates on the sending side of combine to reduce the bytes
+// returned, which may affect precision (pplx accumulates on the receiving
+// side, as moe_combine does).  Send: for each token g and each rank r hosting
+// some of g's experts (e / (E/R) == r), the partial
+//   p[g,r] = bf16(fp32 fma over those copies, ascending j, from +0)
+// goes to slot g*K + j0 (j0 = the rank's first copy).  Receive: the origin adds
+// its partials in ascending rank order in fp32 from +0.
+
+// Token g's copies ordered by (rank, j) in shared memory (thread 0; K <= 32):
+// ord[k] = copy index, first/last mark the ends of each rank's run, slot[k] is
+// the run's first copy.
+struct PartialPlan {
+    int32_t ord[MOE_MAX_TOPK];
+    int32_t slot[MOE_MAX_TOPK];
+    unsigned char first[MOE_MAX_TOPK];
+    unsigned char last[MOE_MAX_TOPK];
+};
+
+__device__ __forceinline__ void plan_partials(const int32_t *idx_g, int K, int L, PartialPlan &pp) {
+    int rank[MOE_MAX_TOPK];
+    for (int j = 0; j < K; ++j) {
+        const int e = idx_g[j];
+        rank[j] = e >= 0 ? e / L : -1;
+        pp.ord[j] = j;
+    }
+    for (int a = 1; a < K; ++a) {   // insertion sort by (rank, j): stable, so j stays ascending
+        const int v = pp.ord[a];
+        int b2 = a - 1;
+        while (b2 >= 0 && rank[pp.ord[b2]] > rank[v]) {
+            pp.ord[b2 + 1] = pp.ord[b2];
+            --b2;
+        }
+        pp.ord[b2 + 1] = v;
+    }
+    int j0 = -1;
+    for (int k = 0; k < K; ++k) {
+        const bool f = k == 0 || rank[pp.ord[k]] != rank[pp.ord[k - 1]];
+        if (f) j0 = pp.ord[k];
+        pp.first[k] = f;
+        pp.last[k] = (k == K - 1) || rank[pp.ord[k + 1]] != rank[pp.ord[k]];
+        pp.slot[k] = j0;
+    }
+}
+
+__global__ void __launch_bounds__(kCombineThreads) combine_partial_send_kernel(
+    const __nv_bfloat16 *__restrict__ y, const int32_t *__restrict__ tok2row, const int32_t *__restrict__ topk_idx,
+    const float *__restrict__ topk_w, int T, int K, int H, int L, long long rows, __nv_bfloat16 *__restrict__ partial) {
+    __shared__ PartialPlan pp;
+    __shared__ int32_t s_row[MOE_MAX_TOPK];
+    __shared__ float s_w[MOE_MAX_TOPK];
+    const int nchunk = H / 8;
+    for (long long g = blockIdx.x; g < T; g += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x < K) {
+            const long long r = __ldg(tok2row + g * K + threadIdx.x);
+            s_row[threadIdx.x] = (r >= 0 && r < rows) ? (int32_t)r : -1;
+            s_w[threadIdx.x] = __ldg(topk_w + g * K + threadIdx.x);
+        }
+        if (threadIdx.x == 0) plan_partials(topk_idx + g * K, K, L, pp);
+        __syncthreads();
+        for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+            float acc[8];
+            for (int k0 = 0; k0 < K; k0 += kCombineBatch) {
+                uint4 v[kCombineBatch];
+#pragma unroll
+                for (int kk = 0; kk < kCombineBatch; ++kk) {
+                    const int k = k0 + kk;
+                    const int r = (k < K) ? s_row[pp.ord[k]] : -1;
+                    v[kk] = (r >= 0) ? ld_stream_v4(y + (size_t)r * H + (size_t)c * 8) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < kCombineBatch; ++kk) {
+                    const int k = k0 + kk;
+                    if (k >= K) break;
+                    if (pp.first[k]) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+                    }
+                    const int j = pp.ord[k];
+                    if (s_row[j] >= 0) {
+                        const float w = s_w[j];
+                        const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v[kk]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = __bfloat1622float2(h2[q]);
+                            acc[2 * q] = __fmaf_rn(w, f.x, acc[2 * q]);
+                            acc[2 * q + 1] = __fmaf_rn(w, f.y, acc[2 * q + 1]);
+                        }
+                    }
+                    if (pp.last[k]) {
+                        uint4 pk;
+                        __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) p2[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+                        st_v4(partial + ((size_t)g * K + pp.slot[k]) * H + (size_t)c * 8, pk);
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <bool kOutF32>
+__global__ void __launch_bounds__(kCombineThreads) combine_partial_recv_kernel(
+    const __nv_bfloat16 *__restrict__ partial, const int32_t *__restrict__ topk_idx, int T, int K, int H, int L,
+    void *__restrict__ out) {
+    __shared__ PartialPlan pp;
+    __shared__ int32_t s_slots[MOE_MAX_TOPK];
+    __shared__ int s_n;
+    const int nchunk = H / 8;
+    for (long long g = blockIdx.x; g < T; g += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            plan_partials(topk_idx + g * K, K, L, pp);
+            int n = 0;
+            for (int k = 0; k < K; ++k)
+                if (pp.first[k] && topk_idx[g * K + pp.ord[k]] >= 0) s_slots[n++] = pp.ord[k];   // ascending rank
+            s_n = n;
+        }
+        __syncthreads();
+        const int n = s_n;
+        for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+            for (int i0 = 0; i0 < n; i0 += kCombineBatch) {
+                uint4 v[kCombineBatch];
+#pragma unroll
+                for (int ii = 0; ii < kCombineBatch; ++ii) {
+                    const int i = i0 + ii;
+                    v[ii] = (i < n) ? ld_stream_v4(partial + ((size_t)g * K + s_slots[i]) * H + (size_t)c * 8)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int ii = 0; ii < kCombineBatch; ++ii) {
+                    if (i0 + ii >= n) break;
+                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v[ii]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 f = __bfloat1622float2(h2[q]);
+                        acc[2 * q] = __fadd_rn(acc[2 * q], f.x);
+                        acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], f.y);
+                    }
+                }
+            }
+            if (kOutF32) {
+                float *o = static_cast<float *>(out) + (size_t)g * H + (size_t)c * 8;
+                st_v4(o, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                                    __float_as_uint(acc[3])));
+                st_v4(o + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]), __float_as_uint(acc[6]),
+                                        __float_as_uint(acc[7])));
+            } else {
+                uint4 pk;
+                __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) p2[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+                st_v4(static_cast<__nv_bfloat16 *>(out) + (size_t)g * H + (size_t)c * 8, pk);
+            }
+        }
+    }
+}
+
+cudaError_t launch_combine_partial(const void *y, const int32_t *tok2row, const int32_t *topk_idx,
+                                   const float *topk_w, int T, int K, int H, int E, int R, void *partial,
+                                   cudaStream_t stream) {
+    long long grid = (long long)device_sm_count() * 16;
+    if (grid > T) grid = T;
+    if (grid < 1) grid = 1;
+    combine_partial_send_kernel<<<(unsigned)grid, kCombineThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(y), tok2row, topk_idx, topk_w, T, K, H, E / R, (long long)T * K,
+        static_cast<__nv_bfloat16 *>(partial));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_partial_recv(const void *partial, const int32_t *topk_idx, int T, int K, int H, int E,
+                                        int R, bool out_f32, void *out, cudaStream_t stream) {
+    long long grid = (long long)device_sm_count() * 16;
+    if (grid > T) grid = T;
+    if (grid < 1) grid = 1;
+    const __nv_bfloat16 *pb = static_cast<const __nv_bfloat16 *>(partial);
+    if (out_f32)
+        combine_partial_recv_kernel<true><<<(unsigned)grid, kCombineThreads, 0, stream>>>(pb, topk_idx, T, K, H, E / R,
+                                                                                          out);
+    else
+        combine_partial_recv_kernel<false><<<(unsigned)grid, kCombineThreads, 0, stream>>>(pb, topk_idx, T, K, H,
+                                                                                           E / R, out);
+    return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -35,6 +35,11 @@ cudaError_t launch_combine(const void *y, const int32_t *tok2row, const float *t
                            bool out_f32, void *out, long long rows, cudaStream_t stream);
 cudaError_t launch_combine_push(const void *y, const int32_t *row2src, const int32_t *counts, int C, int H,
                                 long long rect_rows, long long ret_rows, void *ret, cudaStream_t stream);
+cudaError_t launch_combine_partial(const void *y, const int32_t *tok2row, const int32_t *topk_idx,
+                                   const float *topk_w, int T, int K, int H, int E, int R, void *partial,
+                                   cudaStream_t stream);
+cudaError_t launch_combine_partial_recv(const void *partial, const int32_t *topk_idx, int T, int K, int H, int E,
+                                        int R, bool out_f32, void *out, cudaStream_t stream);
 cudaError_t launch_expert_scale(const void *recv, const float *recv_scale, bool fp8, const int32_t *expert_offsets,
                                 int E, int H, int rows, int identity, void *y, cudaStream_t stream);
 

@@ -335,6 +335,33 @@ MOE_API moe_status moe_combine_ll_push(const void *y, const int32_t *row2src, co
                                        moe_stream_t stream);
 
 /*
+ * moe_combine_partial_send / moe_combine_partial_recv -- combine with
+ * sender-side partial accumulation ([EFA] "Evaluation": DeepEP accumulates on
+ * the sending side to reduce the bytes returned, which may affect precision;
+ * moe_combine accumulates on the receiving side).  Reading implemented (the
+ * page gives no formula): rank r hosts experts e with e / (E/R) == r.
+ *   send: for each token g and each rank r hosting some of g's experts,
+ *         p[g,r] = bf16(fp32 fma over those copies in ascending j, from +0)
+ *         is written to partial row g*K + j0, j0 = the first such copy; other
+ *         rows of partial are not written.  Only one row per (token, rank)
+ *         would travel back instead of one per copy.
+ *   recv: out[g] = fp32 sum of g's partials in ascending rank order from +0,
+ *         then bf16 (nearest even) or fp32.
+ *
+ *   y, tok2row, topk_w  as moe_combine;  topk_idx  device int32 [T, K], the
+ *   routing dispatch used (every entry in [0, E));  E, R as moe_dispatch.
+ *   partial  device bf16 [T*K, H], 16-byte aligned.
+ *   out      device [T, H] of out_dtype (BF16 or FP32), 16-byte aligned.
+ * Errors: MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_CUDA.
+ */
+MOE_API moe_status moe_combine_partial_send(const void *y, const int32_t *tok2row, const int32_t *topk_idx,
+                                            const float *topk_w, int T, int K, int H, int E, int R,
+                                            void *partial, moe_stream_t stream);
+MOE_API moe_status moe_combine_partial_recv(const void *partial, const int32_t *topk_idx, int T, int K, int H,
+                                            int E, int R, moe_dtype out_dtype, void *out,
+                                            moe_stream_t stream);
+
+/*
  * moe_get_device_error -- SYNCHRONOUS: waits for `stream`, then copies the
  * dispatch workspace's error word (an OR of MOE_DEVERR_* bits, 0 if none) to
  * *host_code.  Returns MOE_ERR_TIMEOUT if a timeout bit is set, else
