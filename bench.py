@@ -286,6 +286,55 @@ def measure_partial_combine(b, y, d, idx, wts, out, E, R, K, H, T, stream, flush
         "error_vs_fp64": errs}}
 
 
+def measure_dispatch_overlap(b, x, idx, B, E, fp8, d, H, stream, flush, inter=2048, reps=20):
+    """Dispatch overlapped with a dummy shared expert (the pages' "Dispatch Overlap": the
+    shared expert runs while dispatch moves tokens).  The shared expert stand-in is
+    silu(x W1) W2 with bf16 cuBLAS GEMMs (intermediate size `inter`), on a second stream;
+    reported: each alone, both serialised on one stream, and both on two streams."""
+    gen = torch.Generator(device=x.device).manual_seed(0)
+    w1 = (torch.randn((H, inter), device=x.device, generator=gen) * H ** -0.5).to(torch.bfloat16)
+    w2 = (torch.randn((inter, H), device=x.device, generator=gen) * inter ** -0.5).to(torch.bfloat16)
+    side = torch.cuda.Stream(x.device)
+
+    def shared():
+        return torch.nn.functional.silu(x @ w1) @ w2
+
+    def disp():
+        b.dispatch(x, idx, B, E, fp8=fp8, out=d)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(4)
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            z.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(z) * 1e3)
+        return statistics.median(ts)
+
+    def both_serial():
+        disp()
+        shared()
+
+    def both_overlapped():
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            disp()
+        shared()
+        stream.wait_stream(side)
+
+    res = {"dispatch_us": timed(disp), "shared_expert_us": timed(shared),
+           "serialised_us": timed(both_serial), "overlapped_us": timed(both_overlapped)}
+    res["hidden_frac_of_dispatch"] = (res["serialised_us"] - res["overlapped_us"]) / res["dispatch_us"]
+    return {"dispatch_overlap": {k: round(v, 3) for k, v in res.items()}}
+
+
 def replica_value(per_rank_us: float, world: int) -> float:
     """Whole-job µs per layer for N independent replicas: the slowest rank's
     time per layer divided by the N layers processed in that time."""
@@ -515,6 +564,7 @@ def run_ours(args, world, rank, local):
 
     next_rows.update(measure_decode_layouts(dev, stream, flush))
     next_rows.update(measure_partial_combine(b, y, d, idx, wts, out, E, w.R, K, H, T, stream, flush))
+    next_rows.update(measure_dispatch_overlap(b, x, idx, B, E, w.fp8, d, H, stream, flush))
 
     # correctness of what was timed: the last step's outputs equal the first layer's
     st, code = b.get_device_error(d.workspace)

@@ -49,6 +49,11 @@
 #ifndef MOE_SCATTER_STAGES
 #define MOE_SCATTER_STAGES 3
 #endif
+// SMs the persistent scatter may occupy (0: all of them); fewer leaves room
+// for work running concurrently on another stream.
+#ifndef MOE_SCATTER_MAX_SMS
+#define MOE_SCATTER_MAX_SMS 0
+#endif
 
 namespace moe {
 
@@ -558,7 +563,9 @@ static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, 
         cudaSuccess)
         return ce;
     if (per_sm < 1) per_sm = 1;
-    long long grid = (long long)sm_count() * per_sm;   // persistent: one wave
+    int sms = sm_count();
+    if (MOE_SCATTER_MAX_SMS > 0 && MOE_SCATTER_MAX_SMS < sms) sms = MOE_SCATTER_MAX_SMS;
+    long long grid = (long long)sms * per_sm;   // persistent: one wave
     const long long need = (T + MOE_SCATTER_WARPS - 1) / MOE_SCATTER_WARPS;
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
