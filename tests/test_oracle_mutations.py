@@ -82,10 +82,11 @@ MUTATIONS = [
      "if (v > amax) amax = v;",
      "if (i == 0) amax = v;",
      [F.test_block_quant_matches_library_ops, F.test_block_quant_error_bound_and_amax_code]),
-    ("counts transposed to rank-major",
-     "counts[topk_idx[g * K + j] * R + s] += 1;",
-     "counts[s * E + topk_idx[g * K + j]] += 1;",
-     [P.test_dispatch_matches_library_stable_sort]),
+    ("tokens attributed to the wrong source rank (t mod R)",
+     [("counts[topk_idx[g * K + j] * R + s] += 1;", "counts[topk_idx[g * K + j] * R + (t % R)] += 1;"),
+      ("int32_t row = cursor[e * R + s]++;", "int32_t row = cursor[e * R + (t % R)]++;")],
+     None,
+     [P.test_dispatch_matches_library_stable_sort, P.test_dispatch_brute_force_all_routings]),
     ("rows of a segment in descending token order",
      [("for (int i = 0; i < E * R; ++i) cursor[i] = offsets[i];",
        "for (int i = 0; i < E * R; ++i) cursor[i] = offsets[i + 1];"),
