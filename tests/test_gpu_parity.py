@@ -199,6 +199,7 @@ SHAPES = [
     (16, 32, 4, 1024, [0] * 15 + [900]),       # all tokens on the last rank
     (128, 256, 8, 512, list(range(0, 128))),   # many ranks, ragged
     (256, 256, 6, 128, [i % 5 for i in range(256)]),
+    (8, 1024, 8, 128, [2100] * 8),             # 73728 histogram counts: the decoupled-lookback scan
 ]
 
 

@@ -99,8 +99,9 @@ def _indices_in_bounds(o, rows):
 
 def test_lookback_wait_runs_out_and_reports(gpu, oracle, tmp_path_factory):
     lib = _hooked_library(tmp_path_factory, "MOE_TEST_WITHHOLD_SCAN_BLOCK=0")
-    # E = 1024 experts x 16 tiles = 16384 scan elements: two scan blocks
-    x, idx, B = _inputs(8, 1024, 8, 128, 300, 1, gpu)
+    # E = 1024 experts x 72 tiles = 73728 counts: larger than the histogram kernel scans
+    # itself, so the decoupled-lookback scan runs (9 blocks)
+    x, idx, B = _inputs(8, 1024, 8, 128, 2100, 1, gpu)
     st, code, dt, o = _dispatch_with(lib, x, idx, B, 1024, gpu)
     assert st == TIMEOUT and (code & SCAN_TIMEOUT), (st, code)
     assert 1.0 < dt < 60.0                            # the wait ran for its limit, then returned
