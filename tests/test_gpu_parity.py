@@ -54,12 +54,33 @@ def case(request, gpu, oracle):
     x = inp["x"].to(gpu)
     logits = torch.from_numpy(inp["logits"]).to(gpu)
 
-    idx, wts = b.route_topk(logits, K)
-    d = b.dispatch(x, idx, B, E, fp8=w.fp8)
-    y = b.expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E)
-    out = b.combine(y, d.tok2row, wts)
+    # every output poisoned first (and guard rows past the receive buffer), so that a row
+    # or entry the kernels fail to write cannot pass by holding stale, equal values
+    T = int(np.sum(B))
+    rows = T * K
+    idx = torch.full((T, K), -7, dtype=torch.int32, device=gpu)
+    wts = torch.full((T, K), float("nan"), dtype=torch.float32, device=gpu)
+    b.route_topk(logits, K, topk_idx=idx, topk_w=wts)
+    guard = 64
+    recv_all = torch.full(((rows + guard) * w.H * (1 if w.fp8 else 2),), 0xA5, dtype=torch.uint8, device=gpu)
+    recv = recv_all[: rows * w.H * (1 if w.fp8 else 2)].view(torch.float8_e4m3fn if w.fp8 else torch.bfloat16)
+    d = b.DispatchResult(
+        recv_x=recv.view(rows, w.H),
+        recv_scale=torch.full((rows, w.H // 128), float("nan"), dtype=torch.float32, device=gpu) if w.fp8 else None,
+        counts=torch.full((E * len(B),), -7, dtype=torch.int32, device=gpu),
+        offsets=torch.full((E * len(B) + 1,), -7, dtype=torch.int32, device=gpu),
+        expert_offsets=torch.full((E + 1,), -7, dtype=torch.int32, device=gpu),
+        tok2row=torch.full((rows,), -7, dtype=torch.int32, device=gpu),
+        row2src=torch.full((rows,), -7, dtype=torch.int32, device=gpu),
+        workspace=None)
+    d = b.dispatch(x, idx, B, E, fp8=w.fp8, out=d)
+    y = torch.full((rows, w.H), float("nan"), dtype=torch.bfloat16, device=gpu)
+    b.expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E, out=y)
+    out = torch.full((T, w.H), float("nan"), dtype=torch.bfloat16, device=gpu)
+    b.combine(y, d.tok2row, wts, out=out)
     torch.cuda.synchronize()
     st, code = b.get_device_error(d.workspace)
+    assert bool((recv_all[rows * w.H * (1 if w.fp8 else 2):] == 0xA5).all())   # guard rows untouched
 
     o_idx, o_w = oracle.route_topk(inp["logits"], K)
     od = oracle.dispatch(x_bits, o_idx, B, E, fp8=w.fp8)
