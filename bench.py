@@ -248,6 +248,19 @@ def measure_decode_layouts(dev, stream, flush):
         "ll_combine_push_us": time_flushed(lambda: b.combine_ll_push(yl, dl, R, E, T, K, out=ret), stream, flush),
         "ll_combine_reduce_us": time_flushed(lambda: b.combine(ret, None, wts, out=outl), stream, flush),
     }
+    # CUDA-graph replay of dispatch + combine (one graph per batch size, as the sources deploy it);
+    # the graph is replayed back to back, L2 flushed before each replay outside the events
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        b.dispatch(x, idx, B, E, out=d)
+        b.combine(y, d.tok2row, wts, out=out)
+    gl = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gl):
+        b.dispatch_ll(x, idx, B, E, C, out=dl)
+        b.combine_ll(yl, E, R, C, dl.tok2row, wts, out=outl)
+    torch.cuda.synchronize()
+    res["graph_ragged_dispatch_plus_combine_us"] = time_flushed(g.replay, stream, flush)
+    res["graph_ll_dispatch_plus_combine_us"] = time_flushed(gl.replay, stream, flush)
     db = dispatch_bytes(T, E, R, K, H, False)
     cb = combine_bytes(T, K, H)
     res["floor_us_at_8TBs"] = {"dispatch": db / 8e6, "combine": cb / 8e6}
