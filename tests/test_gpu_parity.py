@@ -221,6 +221,8 @@ SHAPES = [
     (128, 256, 8, 512, list(range(0, 128))),   # many ranks, ragged
     (256, 256, 6, 128, [i % 5 for i in range(256)]),
     (8, 1024, 8, 128, [2100] * 8),             # 73728 histogram counts: the decoupled-lookback scan
+    (1, 1, 1, 16384, [9]),                     # one expert, one rank, the largest hidden size
+    (2, 4, 1, 2048, [0, 37]),                  # K = 1
 ]
 
 
@@ -312,7 +314,8 @@ def test_cuda_graph_replay_matches_eager(gpu):
 # FP8 codec on the device, exhaustively over bf16 inputs
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("amax", [448.0, 224.0, 3.0625])
+@pytest.mark.parametrize("amax", [448.0, 224.0, 3.0625, 1.0, 0.7734375, 2.0**-10, 0.0311279296875, 5.5625,
+                                  17.875, 123.0, 300.0, 447.0])
 def test_fp8_codec_all_bf16_values(amax, gpu, oracle):
     """Every finite bf16 value v with |v| <= amax, quantised in blocks whose
     largest magnitude is amax (for amax = 448 the multiplier is exactly 1, so
