@@ -20,7 +20,9 @@
 // is staged once in shared memory by a bulk copy and written by bulk copies
 // straight into its K destination rows.
 //
-// Three kernels, stream-ordered:
+// Three kernels, stream-ordered (the second and third launched with
+// programmatic stream serialization, so each starts while its predecessor
+// finishes and waits only where it reads the predecessor's output):
 //  1. tile histogram: the items (g, j) of one rank are cut into tiles of
 //     kTileItems consecutive items.  Each warp counts its run of 256 items
 //     into a warp-private shared histogram; lanes holding the same expert are
@@ -34,8 +36,12 @@
 //     are rank-major and ranks hold consecutive tokens, this order is exactly
 //     (expert, source rank, token): the scanned value of (e, tile) is the
 //     first receive row of expert e's items in that tile.
-//  3. scatter: row(g, j) = scan[e * ntiles + tile(g, j)] + rank-in-tile;
-//     copy (or quantise once and copy) x[g] into its K rows.
+//  3. scatter, one warp per token: row(g, j) = scan[e * ntiles + tile(g, j)]
+//     + rank-in-tile; copy (or quantise once and copy) x[g] into its K rows.
+//
+// The low-latency layout (lehuy.net, same article, "Optimising for latency:
+// send without asking") skips the scan: its rows are a static formula over a
+// fixed region per (expert, source rank), so it runs kernels 1 and 3 only.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -264,7 +270,6 @@ struct ScatterArgs {
     const int32_t *tile_hist;  // [E * ntiles] (low-latency layout)
     int T, E, K, H;
     int C;                     // low-latency layout: rows per (expert, source rank) region
-    int stages;
 };
 
 // 16 lanes quantise one 128-channel block: lane owns 8 consecutive channels.
@@ -553,7 +558,6 @@ static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, 
     const int H = a.H;
     cudaError_t ce;
     const size_t smem = scatter_stage_bytes(H, fp8) * MOE_SCATTER_STAGES * MOE_SCATTER_WARPS;
-    a.stages = MOE_SCATTER_STAGES;
     const void *kfn = fp8 ? (ll ? (const void *)scatter_kernel<true, true> : (const void *)scatter_kernel<true, false>)
                           : (ll ? (const void *)scatter_kernel<false, true> : (const void *)scatter_kernel<false, false>);
     if ((ce = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
