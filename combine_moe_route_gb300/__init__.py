@@ -18,7 +18,7 @@ _API = {
     "combine_partial_send", "combine_partial_recv",
 }
 
-__all__ = sorted(_API) + ["workloads"]
+__all__ = sorted(_API) + ["workloads", "HostLayerPipeline"]
 
 
 def __getattr__(name):
@@ -26,4 +26,6 @@ def __getattr__(name):
         return getattr(import_module(".binding", __name__), name)
     if name == "workloads":
         return import_module(".workloads", __name__)
+    if name == "HostLayerPipeline":
+        return import_module(".pipeline", __name__).HostLayerPipeline
     raise AttributeError(name)
