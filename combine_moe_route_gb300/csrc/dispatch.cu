@@ -26,9 +26,10 @@
 //  1. tile histogram: the items (g, j) of one rank are cut into tiles of
 //     kTileItems consecutive items.  Each warp counts its run of 256 items
 //     into a warp-private shared histogram; lanes holding the same expert are
-//     grouped with __match_any_sync and their leader adds the group size with
-//     one shared-memory atomic, whose return value plus the lane's position in
-//     the group is the item's rank among equal experts so far.  The warps'
+//     grouped by a ballot per bit of the expert id and their leader adds the
+//     group size with one shared-memory atomic, whose return value plus the
+//     lane's position in the group is the item's rank among equal experts so
+//     far.  The warps'
 //     histograms are then combined in warp order, giving every item a stable
 //     rank inside (expert, tile) and every tile its per-expert total.
 //  2. exclusive scan over the histogram laid out expert-major, tile-minor
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
 
     int32_t *my_hist = hist + warp * E;
     const unsigned lanemask_lt = (1u << lane) - 1u;
+    const int ebits = (E > 1) ? 32 - __clz(E - 1) : 0;   // bits of the largest expert id
     int e_reg[kItemsPerThread];
     int r_reg[kItemsPerThread];
     int bad = 0;
@@ -106,9 +108,15 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
             bad = 1;
             e = -1;
         }
-        // invalid lanes get distinct negative keys so they never form a group with a valid lane
-        const int key = (e >= 0) ? e : -1 - lane;
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        // lanes holding the same expert: one ballot per bit of the expert id
+        // (a multi-split; its cost does not grow with the number of distinct
+        // experts in the warp, unlike a match instruction)
+        unsigned peers = __ballot_sync(0xffffffffu, e >= 0);
+        for (int b = 0; b < ebits; ++b) {
+            const bool bit = (e >> b) & 1;
+            const unsigned m = __ballot_sync(0xffffffffu, bit);
+            peers &= bit ? m : ~m;
+        }
         int r = -1;
         if (e >= 0) {
             const int leader = __ffs(peers) - 1;
