@@ -194,17 +194,27 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
     pdl_wait();                                    // the tile histogram is complete and visible
     __syncthreads();
     const int vid = s_vid;
-    const long long base = (long long)vid * kScanChunk + (long long)tid * kScanPerThread;
+    // warp w owns kScanPerThread consecutive 32-element slices of the block's
+    // chunk; slice k is read and written by the 32 lanes together (coalesced)
+    const long long wbase = (long long)vid * kScanChunk + (long long)warp * (32 * kScanPerThread);
 
     int v[kScanPerThread];
-    int sum = 0;
+    int incl[kScanPerThread];   // inclusive scan inside slice k
 #pragma unroll
     for (int k = 0; k < kScanPerThread; ++k) {
-        v[k] = (base + k < n) ? in[base + k] : 0;
-        sum += v[k];
+        const long long i = wbase + k * 32 + lane;
+        v[k] = (i < n) ? in[i] : 0;
     }
-    const int incl = warp_inclusive_scan(sum);
-    if (lane == 31) s_warp[warp] = incl;
+#pragma unroll
+    for (int k = 0; k < kScanPerThread; ++k) incl[k] = warp_inclusive_scan(v[k]);
+    int slice_excl[kScanPerThread];   // sum of the warp's earlier slices
+    int wsum = 0;
+#pragma unroll
+    for (int k = 0; k < kScanPerThread; ++k) {
+        slice_excl[k] = wsum;
+        wsum += __shfl_sync(0xffffffffu, incl[k], 31);
+    }
+    if (lane == 0) s_warp[warp] = wsum;
     __syncthreads();
     if (warp == 0) {
         const int wv = (lane < kScanThreads / 32) ? s_warp[lane] : 0;
@@ -220,8 +230,8 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
 #else
             const bool publish = true;
 #endif
+            // a status word carries its own value, so publishing needs no fence
             if (vid == 0) {
-                __threadfence();
                 if (publish) atomicExch(&status[0], kFlagPrefix | (unsigned long long)(unsigned)aggregate);
             } else {
                 if (publish) atomicExch(&status[vid], kFlagAgg | (unsigned long long)(unsigned)aggregate);
@@ -244,7 +254,6 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
                     --p;
                 }
                 if (timed_out) set_device_error(err, MOE_DEVERR_SCAN_TIMEOUT);
-                __threadfence();
                 if (publish) atomicExch(&status[vid], kFlagPrefix | (unsigned long long)(unsigned)(excl + aggregate));
             }
             s_excl = excl;
@@ -252,11 +261,11 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
         }
     }
     __syncthreads();
-    int run = s_excl + s_warp[warp] + (incl - sum);
+    const int wexcl = s_excl + s_warp[warp];
 #pragma unroll
     for (int k = 0; k < kScanPerThread; ++k) {
-        if (base + k < n) out[base + k] = run;
-        run += v[k];
+        const long long i = wbase + k * 32 + lane;
+        if (i < n) out[i] = wexcl + slice_excl[k] + incl[k] - v[k];
     }
 }
 
@@ -276,6 +285,7 @@ struct ScatterArgs {
     int32_t *row2src;
     int32_t *err;
     const int32_t *tile_hist;  // [E * ntiles] (low-latency layout)
+    int32_t *next_token;       // token counter, zero at launch (workspace header)
     int T, E, K, H;
     int C;                     // low-latency layout: rows per (expert, source rank) region
 };
@@ -318,19 +328,47 @@ __host__ __device__ inline size_t scatter_stage_bytes(int H, bool fp8) {
     return (b + 127) & ~(size_t)127;
 }
 
-// Persistent, one warp per token: warp w of the grid takes tokens
-// g = w, w + W, w + 2W, ... (W = warps in the grid) and runs its own ring of
-// S bulk-copy stages, so warps never wait on one another.  Per token:
+// Quantise one staged bf16 row to e4m3 in place (its H/128 fp32 scales after
+// the row's 2H bytes): two 128-channel blocks per step (16 lanes per block),
+// ascending, so every e4m3 byte lands on bf16 bytes that have already been read.
+__device__ __forceinline__ void quantize_stage(unsigned char *buf, int H, int lane) {
+    const int nblk = H / 128;
+    float *sc = reinterpret_cast<float *>(buf + (size_t)H * 2);
+    const uint4 *src = reinterpret_cast<const uint4 *>(buf);
+    uint2 *q = reinterpret_cast<uint2 *>(buf);
+    const int hl = lane & 15;
+    for (int b0 = 0; b0 < nblk; b0 += 2) {
+        const int b = b0 + (lane >> 4);
+        const bool valid = b < nblk;
+        const uint4 xin = valid ? src[b * 16 + hl] : make_uint4(0u, 0u, 0u, 0u);
+        uint2 qo;
+        float s;
+        quantize_block16(xin, qo, s);   // its shuffles order every lane's read before any write
+        if (valid) {
+            q[b * 16 + hl] = qo;
+            if (hl == 0) sc[b] = s;
+        }
+    }
+    fence_proxy_async_smem();
+}
+
+// Persistent, one warp per token.  Warp w starts with tokens w, w + W, ...,
+// w + (S-1)W (W warps in the grid); after those, lane 0 claims each further
+// token from a counter in the (zeroed) workspace header, so warps on faster
+// SMs take more tokens and the grid ends together.  Each warp runs its own
+// ring of S bulk-copy stages; its token sequence number it selects stage
+// it % S.  Before waiting for the scan, a warp loads its first S tokens and
+// (FP8) quantises the first one, none of which depends on the histogram.
+// Per token:
 //   1. lanes j < K compute the destination row of copy j (scan base of the
 //      token's tile + its in-tile rank) and write tok2row / row2src;
 //   2. wait for the staged source row (mbarrier, bounded);
-//   3. FP8: quantise in place, two 128-channel blocks per step (16 lanes per
-//      block), ascending, so every e4m3 byte lands on bf16 bytes that have
-//      already been read;
+//   3. FP8: quantise in place;
 //   4. lane 0 issues K bulk stores of the row (and, when H % 512 == 0, K bulk
 //      stores of the scale row; otherwise the lanes store the scales);
 //   5. once the previous token's stores have read their stage, lane 0 refills
-//      that stage with the token S - 1 ahead.
+//      that stage with a newly claimed token (claimed one token in advance, so
+//      the atomic's latency is hidden behind the current token).
 //
 // kLL (low-latency layout): the destination is a fixed rectangle with C rows
 // per (expert, source rank) region; row = (e*R + s)*C + (tokens of rank s
@@ -341,6 +379,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bars[MOE_SCATTER_WARPS][MOE_SCATTER_STAGES];
     __shared__ int32_t s_rows[MOE_SCATTER_WARPS][MOE_MAX_TOPK];
+    __shared__ int32_t s_tok[MOE_SCATTER_WARPS][MOE_SCATTER_STAGES];   // token held by each stage
     constexpr int S = MOE_SCATTER_STAGES;
     static_assert(S >= 2, "the refill schedule needs at least two stages per warp");
 
@@ -354,31 +393,49 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
     const size_t recv_pitch = kFp8 ? (size_t)H : (size_t)H * 2;
     const bool scale_bulk = kFp8 && (nblk * 4) % 16 == 0;
 
-    const long long W = (long long)gridDim.x * MOE_SCATTER_WARPS;
-    const long long gw = (long long)blockIdx.x * MOE_SCATTER_WARPS + warp;
-    const int my_count = (gw < T) ? (int)((T - 1 - gw) / W + 1) : 0;
     unsigned char *wbase = smem + (size_t)warp * S * stage_bytes;
     auto stage = [&](int it) { return wbase + (size_t)(it % S) * stage_bytes; };
-    auto token_of = [&](int it) { return gw + (long long)it * W; };
+    // the first S tokens of warp w are w, w + W, ..., w + (S-1)W (W warps in
+    // the grid), which spreads a small batch over every warp; the tokens from
+    // S*W on are handed out by the counter
+    const long long W = (long long)gridDim.x * MOE_SCATTER_WARPS;
+    const long long gw = (long long)blockIdx.x * MOE_SCATTER_WARPS + warp;
+    const long long first_dynamic = (long long)S * W;
 
     // prologue: the source rows do not depend on the histogram or the scan,
-    // so their loads go out before waiting for the previous kernel
-    int loads_issued = 0;
-    if (lane == 0 && my_count > 0) {
+    // so the first S tokens are loaded before waiting for it
+    int claimed = 0;      // tokens this warp has claimed and started loading
+    long long next_g = T;   // lane 0: the token claimed in advance for the next refill
+    if (lane == 0) {
         for (int st = 0; st < S; ++st) mbar_init(&bars[warp][st], 1);
         fence_proxy_async_smem();
-        loads_issued = min(S, my_count);
-        for (int it = 0; it < loads_issued; ++it) {
-            mbar_arrive_expect_tx(&bars[warp][it], in_bytes);
+        for (; claimed < S && gw + (long long)claimed * W < T; ++claimed) {
+            const int g = (int)(gw + (long long)claimed * W);
+            s_tok[warp][claimed] = g;
+            mbar_arrive_expect_tx(&bars[warp][claimed], in_bytes);
 #ifdef MOE_TEST_WITHHOLD_FIRST_LOAD
-            // Test builds only: the grid's first warp arms its first stage but never
+            // Test builds only: the warp holding token 0 arms its stage but never
             // issues the copy, so its bounded barrier wait runs out.
-            if (gw == 0 && it == 0) continue;
+            if (g == 0) continue;
 #endif
-            bulk_load(stage(it), a.x + token_of(it) * H, in_bytes, &bars[warp][it]);
+            bulk_load(stage(claimed), a.x + (long long)g * H, in_bytes, &bars[warp][claimed]);
+        }
+        if (claimed == S) next_g = first_dynamic + atomicAdd(a.next_token, 1);
+    }
+    claimed = __shfl_sync(0xffffffffu, claimed, 0);
+    __syncwarp();
+
+    int failed_at = -1;
+    bool first_quantised = false;
+    if (kFp8 && claimed > 0) {
+        if (__all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][0], 0u))) {
+            quantize_stage(stage(0), H, lane);
+            first_quantised = true;
+        } else {
+            if (lane == 0) set_device_error(a.err, MOE_DEVERR_COPY_TIMEOUT);
+            failed_at = 0;
         }
     }
-    __syncwarp();
     pdl_wait();
 
     if (kLL) {
@@ -410,15 +467,14 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
             }
         }
     }
-    if (my_count == 0) return;
+    if (claimed == 0) return;
 
-    int failed_at = -1;
-    for (int it = 0; it < my_count; ++it) {
+    for (int it = 0; failed_at < 0 && it < claimed; ++it) {
         const uint32_t parity = (uint32_t)((it / S) & 1);
         unsigned char *buf = stage(it);
         // 1. destination rows (lane j = copy j)
         {
-            const long long g = token_of(it);
+            const long long g = s_tok[warp][it % S];
             const int sidx = upper_bound_minus_one(rt.rank_off, rt.R, (int32_t)g);
             const long long item0 = (long long)rt.rank_off[sidx] * K;
             int e = -1, row = -1;
@@ -461,24 +517,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
 
         // 3. quantise in place
         float *sc = reinterpret_cast<float *>(buf + (size_t)H * 2);
-        if (kFp8) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(buf);
-            uint2 *q = reinterpret_cast<uint2 *>(buf);
-            const int hl = lane & 15;
-            for (int b0 = 0; b0 < nblk; b0 += 2) {
-                const int b = b0 + (lane >> 4);
-                const bool valid = b < nblk;
-                const uint4 xin = valid ? src[b * 16 + hl] : make_uint4(0u, 0u, 0u, 0u);
-                uint2 qo;
-                float s;
-                quantize_block16(xin, qo, s);   // its shuffles order every lane's read before any write
-                if (valid) {
-                    q[b * 16 + hl] = qo;
-                    if (hl == 0) sc[b] = s;
-                }
-            }
-            fence_proxy_async_smem();
-        }
+        if (kFp8 && !(it == 0 && first_quantised)) quantize_stage(buf, H, lane);
         __syncwarp();
 
         // 4. K bulk stores from the stage
@@ -500,15 +539,19 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
             }
         }
 
-        // 5. refill the previous token's stage once its stores have read it
-        if (lane == 0 && it >= 1 && it - 1 + S < my_count) {
+        // 5. refill the previous token's stage (sequence number it - 1 + S ==
+        //    claimed, the ring being full) once its stores have read it
+        if (lane == 0 && it >= 1 && next_g < T) {
             bulk_wait_read<1>();
-            const int nxt = it - 1 + S;
+            const int nxt = claimed;
+            s_tok[warp][nxt % S] = (int32_t)next_g;
             mbar_arrive_expect_tx(&bars[warp][nxt % S], in_bytes);
-            bulk_load(stage(nxt), a.x + token_of(nxt) * H, in_bytes, &bars[warp][nxt % S]);
-            loads_issued = nxt + 1;
+            bulk_load(stage(nxt), a.x + (long long)next_g * H, in_bytes, &bars[warp][nxt % S]);
+            ++claimed;
+            next_g = first_dynamic + atomicAdd(a.next_token, 1);
         }
-        __syncwarp();   // s_rows and the stage are reused S tokens later
+        __syncwarp();   // s_rows, s_tok and the stage are reused in later iterations
+        claimed = __shfl_sync(0xffffffffu, claimed, 0);
     }
 
     if (lane == 0) {
@@ -516,7 +559,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
             // let every load this warp issued land before the block's shared
             // memory goes away (each wait is bounded; one that never arrives
             // costs its limit and the rest are still waited for)
-            for (int t = failed_at; t < loads_issued; ++t)
+            for (int t = failed_at; t < claimed; ++t)
                 (void)mbar_wait_bounded(&bars[warp][t % S], (uint32_t)((t / S) & 1));
         }
         bulk_wait_all();
@@ -610,12 +653,12 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
     const DispatchPlan p = plan_dispatch(E, rt.ntiles);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     int32_t *err = reinterpret_cast<int32_t *>(ws);
-    int32_t *ticket = reinterpret_cast<int32_t *>(ws + 4);
+    int32_t *ticket = reinterpret_cast<int32_t *>(ws + 4);   // scan block start order
     unsigned long long *status = reinterpret_cast<unsigned long long *>(ws + p.off_status);
     int32_t *tile_hist = reinterpret_cast<int32_t *>(ws + p.off_hist);
     int32_t *scan = reinterpret_cast<int32_t *>(ws + p.off_scan);
 
-    cudaError_t ce = cudaMemsetAsync(ws, 0, p.off_hist, stream);   // error word, ticket, lookback flags
+    cudaError_t ce = cudaMemsetAsync(ws, 0, p.off_hist, stream);   // error word, ticket, token counter, lookback flags
     if (ce != cudaSuccess) return ce;
 
     const size_t hist_smem = (size_t)kHistWarps * E * 4;
@@ -650,6 +693,7 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
     a.tok2row = tok2row;
     a.row2src = row2src;
     a.err = err;
+    a.next_token = reinterpret_cast<int32_t *>(ws + 8);   // scatter token counter
     a.T = (int)T;
     a.E = E;
     a.K = K;
@@ -666,7 +710,7 @@ cudaError_t launch_dispatch_ll(const void *x, const int32_t *topk_idx, const Ran
     int32_t *err = reinterpret_cast<int32_t *>(ws);
     int32_t *tile_hist = reinterpret_cast<int32_t *>(ws + p.off_hist);
 
-    cudaError_t ce = cudaMemsetAsync(ws, 0, kWsHeader, stream);   // error word
+    cudaError_t ce = cudaMemsetAsync(ws, 0, kWsHeader, stream);   // error word, token counter
     if (ce != cudaSuccess) return ce;
     const size_t hist_smem = (size_t)kHistWarps * E * 4;
     tile_hist_kernel<<<rt.ntiles, kHistThreads, hist_smem, stream>>>(topk_idx, E, K, rt, tile_hist, tok2row, err);
@@ -681,6 +725,7 @@ cudaError_t launch_dispatch_ll(const void *x, const int32_t *topk_idx, const Ran
     a.tok2row = tok2row;
     a.row2src = row2src;
     a.err = err;
+    a.next_token = reinterpret_cast<int32_t *>(ws + 8);   // scatter token counter
     a.tile_hist = tile_hist;
     a.T = (int)T;
     a.E = E;
