@@ -54,7 +54,7 @@
 #define MOE_SCATTER_WARPS 1
 #endif
 #ifndef MOE_SCATTER_STAGES
-#define MOE_SCATTER_STAGES 3
+#define MOE_SCATTER_STAGES 2
 #endif
 // SMs the persistent scatter may occupy (0: all of them); fewer leaves room
 // for work running concurrently on another stream.
