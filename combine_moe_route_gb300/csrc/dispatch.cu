@@ -46,6 +46,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <mutex>
+
 #include "launch.h"
 
 // Scatter launch shape (tunable at build time; the defaults are the measured best):
@@ -117,16 +119,15 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
             const unsigned m = __ballot_sync(0xffffffffu, bit);
             peers &= bit ? m : ~m;
         }
-        int r = -1;
-        if (e >= 0) {
-            const int leader = __ffs(peers) - 1;
-            int base = 0;
-            if (lane == leader) base = atomicAdd(&my_hist[e], __popc(peers));
-            base = __shfl_sync(peers, base, leader);
-            r = base + __popc(peers & lanemask_lt);
-        }
+        // the group's lowest lane adds the group size; every lane then reads
+        // its own group leader's old count in one full-warp shuffle (a
+        // shuffle masked by the group would run once per distinct expert)
+        const int leader = (e >= 0) ? __ffs(peers) - 1 : lane;
+        int base = 0;
+        if (e >= 0 && lane == leader) base = atomicAdd(&my_hist[e], __popc(peers));
+        base = __shfl_sync(0xffffffffu, base, leader);
         e_reg[step] = e;
-        r_reg[step] = r;
+        r_reg[step] = (e >= 0) ? base + __popc(peers & lanemask_lt) : -1;
         __syncwarp();
     }
     if (bad) set_device_error(err, MOE_DEVERR_EXPERT_RANGE);
@@ -602,6 +603,46 @@ static int sm_count() {
 
 int device_sm_count() { return sm_count(); }
 
+// Blocks per SM of a scatter variant at a dynamic shared-memory size on the
+// current device.  The kernel's shared-memory limit is only ever raised and the
+// occupancy is asked once per (kernel, device, size): both are host calls that
+// would otherwise sit on every launch's critical path.
+static cudaError_t scatter_blocks_per_sm(const void *kfn, size_t smem, int *per_sm) {
+    struct Limit { const void *fn; int dev; size_t smem; };
+    struct Occ { const void *fn; int dev; size_t smem; int per_sm; };
+    static std::mutex mu;
+    static Limit limits[16];
+    static int nlimits = 0;
+    static Occ occs[64];
+    static int noccs = 0;
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return ce;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < noccs; ++i)
+        if (occs[i].fn == kfn && occs[i].dev == dev && occs[i].smem == smem) {
+            *per_sm = occs[i].per_sm;
+            return cudaSuccess;
+        }
+    int li = -1;
+    for (int i = 0; i < nlimits; ++i)
+        if (limits[i].fn == kfn && limits[i].dev == dev) li = i;
+    if (li < 0 || limits[li].smem < smem) {
+        if ((ce = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+            return ce;
+        if (li >= 0)
+            limits[li].smem = smem;
+        else if (nlimits < 16)
+            limits[nlimits++] = Limit{kfn, dev, smem};
+    }
+    int n = 0;
+    if ((ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kfn, MOE_SCATTER_WARPS * 32, smem)) != cudaSuccess)
+        return ce;
+    if (noccs < 64) occs[noccs++] = Occ{kfn, dev, smem, n};
+    *per_sm = n;
+    return cudaSuccess;
+}
+
 // Persistent launch of the scatter (one wave), with programmatic stream
 // serialization so that it stages its first rows while the previous kernel ends.
 static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, bool ll, cudaStream_t stream) {
@@ -611,12 +652,8 @@ static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, 
     const size_t smem = scatter_stage_bytes(H, fp8) * MOE_SCATTER_STAGES * MOE_SCATTER_WARPS;
     const void *kfn = fp8 ? (ll ? (const void *)scatter_kernel<true, true> : (const void *)scatter_kernel<true, false>)
                           : (ll ? (const void *)scatter_kernel<false, true> : (const void *)scatter_kernel<false, false>);
-    if ((ce = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
-        return ce;
     int per_sm = 0;
-    if ((ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, MOE_SCATTER_WARPS * 32, smem)) !=
-        cudaSuccess)
-        return ce;
+    if ((ce = scatter_blocks_per_sm(kfn, smem, &per_sm)) != cudaSuccess) return ce;
     if (per_sm < 1) per_sm = 1;
     int sms = sm_count();
     if (MOE_SCATTER_MAX_SMS > 0 && MOE_SCATTER_MAX_SMS < sms) sms = MOE_SCATTER_MAX_SMS;
