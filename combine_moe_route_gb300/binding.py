@@ -103,13 +103,15 @@ def _stream_handle(stream, device) -> int:
 
 
 def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> torch.Tensor:
+    # on every call's path: attribute checks only (no device objects or tuple copies)
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
+    if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (got {t.device}); there is no CPU path")
-    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
-        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if dtype is not None:
+        if (t.dtype not in dtype) if type(dtype) is tuple else (t.dtype is not dtype):
+            raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if shape is not None and t.shape != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
