@@ -221,7 +221,8 @@ def time_flushed(fn, stream, flush, reps: int = 50) -> float:
 def measure_decode_layouts(dev, stream, flush):
     """DeepSeek-V3 decode layer (R=8, E=256, K=8, H=7168, 128 tokens/rank, bf16): dispatch and
     combine through the throughput (ragged) layout and through the low-latency rectangle
-    (chunk cap C = 128), each call timed on its own with the L2 flushed."""
+    (chunk cap C = 128; slots in token order, or taken by atomic increments), each call timed on
+    its own with the L2 flushed."""
     from combine_moe_route_gb300 import binding as b
     from combine_moe_route_gb300 import workloads as wl
     w = wl.WORKLOADS["dsv3_decode"]
@@ -238,11 +239,16 @@ def measure_decode_layouts(dev, stream, flush):
     yl = b.expert_scale(dl.recv_x, None, eo, E)
     outl = b.combine_ll(yl, E, R, C, dl.tok2row, wts)
     ret = b.combine_ll_push(yl, dl, R, E, T, K)
+    du = b.dispatch_ll(x, idx, B, E, C, unordered=True)      # slots by atomic increments, no histogram
+    yu = b.expert_scale(du.recv_x, None, eo, E)
+    outu = b.combine_ll(yu, E, R, C, du.tok2row, wts)
     torch.cuda.synchronize()
     res = {
         "ragged_dispatch_us": time_flushed(lambda: b.dispatch(x, idx, B, E, out=d), stream, flush),
         "ragged_combine_us": time_flushed(lambda: b.combine(y, d.tok2row, wts, out=out), stream, flush),
         "ll_dispatch_us": time_flushed(lambda: b.dispatch_ll(x, idx, B, E, C, out=dl), stream, flush),
+        "ll_unordered_dispatch_us": time_flushed(
+            lambda: b.dispatch_ll(x, idx, B, E, C, unordered=True, out=du), stream, flush),
         "ll_combine_gather_us": time_flushed(lambda: b.combine_ll(yl, E, R, C, dl.tok2row, wts, out=outl),
                                              stream, flush),
         "ll_combine_push_us": time_flushed(lambda: b.combine_ll_push(yl, dl, R, E, T, K, out=ret), stream, flush),
@@ -258,9 +264,14 @@ def measure_decode_layouts(dev, stream, flush):
     with torch.cuda.graph(gl):
         b.dispatch_ll(x, idx, B, E, C, out=dl)
         b.combine_ll(yl, E, R, C, dl.tok2row, wts, out=outl)
+    gu = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gu):
+        b.dispatch_ll(x, idx, B, E, C, unordered=True, out=du)
+        b.combine_ll(yu, E, R, C, du.tok2row, wts, out=outu)
     torch.cuda.synchronize()
     res["graph_ragged_dispatch_plus_combine_us"] = time_flushed(g.replay, stream, flush)
     res["graph_ll_dispatch_plus_combine_us"] = time_flushed(gl.replay, stream, flush)
+    res["graph_ll_unordered_dispatch_plus_combine_us"] = time_flushed(gu.replay, stream, flush)
     db = dispatch_bytes(T, E, R, K, H, False)
     cb = combine_bytes(T, K, H)
     res["floor_us_at_8TBs"] = {"dispatch": db / 8e6, "combine": cb / 8e6}

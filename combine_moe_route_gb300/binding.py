@@ -70,6 +70,9 @@ def load_library() -> ctypes.CDLL:
         lib.moe_combine.restype = i32
         lib.moe_dispatch_ll.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.moe_dispatch_ll.restype = i32
+        lib.moe_dispatch_ll_unordered.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                                  sz, vp]
+        lib.moe_dispatch_ll_unordered.restype = i32
         lib.moe_combine_ll.argtypes = [vp, i32, i32, i32, vp, vp, i32, i32, i32, i32, vp, vp]
         lib.moe_combine_ll.restype = i32
         lib.moe_combine_ll_push.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
@@ -324,8 +327,12 @@ class DispatchLLResult:
 
 
 def dispatch_ll(x: torch.Tensor, topk_idx: torch.Tensor, B, E: int, C: int, *, fp8: bool = False,
-                out: DispatchLLResult | None = None, stream=None) -> DispatchLLResult:
-    """Low-latency dispatch into a fixed [E*R*C, H] rectangle (C rows per (expert, rank) region)."""
+                unordered: bool = False, out: DispatchLLResult | None = None, stream=None) -> DispatchLLResult:
+    """Low-latency dispatch into a fixed [E*R*C, H] rectangle (C rows per (expert, rank) region).
+
+    unordered=True: each copy takes its slot in its region by an atomic increment
+    (moe_dispatch_ll_unordered): no histogram pass, and the order of the rows inside
+    a region is unspecified."""
     _dev(x, "x", torch.bfloat16)
     T, H = x.shape
     _dev(topk_idx, "topk_idx", torch.int32)
@@ -345,12 +352,14 @@ def dispatch_ll(x: torch.Tensor, topk_idx: torch.Tensor, B, E: int, C: int, *, f
             row2src=torch.empty(rows, dtype=torch.int32, device=dev),
             workspace=torch.empty(max(dispatch_workspace_bytes(R, E, K, T), 256), dtype=torch.uint8, device=dev),
             C=C)
+    lib = load_library()
+    fn, name = ((lib.moe_dispatch_ll_unordered, "moe_dispatch_ll_unordered") if unordered
+                else (lib.moe_dispatch_ll, "moe_dispatch_ll"))
     with torch.cuda.device(dev):
-        _check(load_library().moe_dispatch_ll(
+        _check(fn(
             _ptr(x), _ptr(topk_idx), R, Bh.ctypes.data, E, K, H, C, _DTYPE_FP8 if fp8 else _DTYPE_BF16,
             _ptr(out.recv_x), _ptr(out.recv_scale) if fp8 else None, _ptr(out.counts), _ptr(out.tok2row),
-            _ptr(out.row2src), _ptr(out.workspace), out.workspace.numel(), _stream_handle(stream, dev)),
-            "moe_dispatch_ll")
+            _ptr(out.row2src), _ptr(out.workspace), out.workspace.numel(), _stream_handle(stream, dev)), name)
     return out
 
 

@@ -171,6 +171,34 @@ moe_status moe_dispatch_ll(const void *x, const int32_t *topk_idx, int R, const 
                                                counts, tok2row, row2src, workspace, st));
 }
 
+moe_status moe_dispatch_ll_unordered(const void *x, const int32_t *topk_idx, int R, const int32_t *B, int E, int K,
+                                     int H, int C, moe_dtype recv_dtype, void *recv_x, float *recv_scale,
+                                     int32_t *counts, int32_t *tok2row, int32_t *row2src, void *workspace,
+                                     size_t workspace_bytes, moe_stream_t stream) {
+    if (R < 1 || R > MOE_MAX_RANKS || !B || !topk_shape_ok(E, K) || E % R != 0) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (recv_dtype != MOE_DTYPE_BF16 && recv_dtype != MOE_DTYPE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = recv_dtype == MOE_DTYPE_FP8_E4M3;
+    if (fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (C < 1 || (long long)E * R * C >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+    moe::RankTable rt;
+    long long T = 0;
+    if (!build_rank_table(R, B, K, rt, T)) return MOE_ERR_INVALID_ARG;
+    for (int s = 0; s < R; ++s)
+        if (B[s] > C) return MOE_ERR_INVALID_ARG;   // the chunk cap bounds every region
+    if (!counts) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) return cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E * R, st));
+    if (!x || !topk_idx || !recv_x || !tok2row || !row2src || (fp8 && !recv_scale)) return MOE_ERR_INVALID_ARG;
+    if (!workspace) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < moe::kWsHeader) return MOE_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(recv_x) || !aligned16(workspace) || (fp8 && !aligned16(recv_scale)))
+        return MOE_ERR_UNSUPPORTED;
+    return cuda_status(moe::launch_dispatch_ll_unordered(x, topk_idx, rt, E, K, H, C, fp8, recv_x,
+                                                         fp8 ? recv_scale : nullptr, counts, tok2row, row2src,
+                                                         workspace, st));
+}
+
 moe_status moe_combine_ll(const void *y, int E, int R, int C, const int32_t *tok2row, const float *topk_w, int T,
                           int K, int H, moe_dtype out_dtype, void *out, moe_stream_t stream) {
     if (T < 0 || K < 1 || K > MOE_MAX_TOPK || E < 1 || R < 1 || C < 1) return MOE_ERR_INVALID_ARG;

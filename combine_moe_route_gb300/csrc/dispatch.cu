@@ -371,10 +371,16 @@ __device__ __forceinline__ void quantize_stage(unsigned char *buf, int H, int la
 //      that stage with a newly claimed token (claimed one token in advance, so
 //      the atomic's latency is hidden behind the current token).
 //
-// kLL (low-latency layout): the destination is a fixed rectangle with C rows
-// per (expert, source rank) region; row = (e*R + s)*C + (tokens of rank s
-// routed to e in the rank's earlier tiles) + in-tile rank.  No scan is needed.
-template <bool kFp8, bool kLL>
+// kLowLatency: the destination is a fixed rectangle with C rows per (expert,
+// source rank) region; row = (e*R + s)*C + (tokens of rank s routed to e in
+// the rank's earlier tiles) + in-tile rank.  No scan is needed.
+// kLowLatencyUnordered: the same rectangle, but a copy takes its slot in the
+// region by one atomic increment of the region's count (zeroed before the
+// launch), so neither histogram nor scan runs; the order of a region's rows is
+// whatever order the increments happened in.
+enum ScatterMode : int { kRagged = 0, kLowLatency = 1, kLowLatencyUnordered = 2 };
+
+template <bool kFp8, int kMode>
 __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const ScatterArgs a,
                                                                          const __grid_constant__ RankTable rt) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -421,7 +427,6 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
 #endif
             bulk_load(stage(claimed), a.x + (long long)g * H, in_bytes, &bars[warp][claimed]);
         }
-        if (claimed == S) next_g = first_dynamic + atomicAdd(a.next_token, 1);
     }
     claimed = __shfl_sync(0xffffffffu, claimed, 0);
     __syncwarp();
@@ -433,13 +438,18 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
             quantize_stage(stage(0), H, lane);
             first_quantised = true;
         } else {
-            if (lane == 0) set_device_error(a.err, MOE_DEVERR_COPY_TIMEOUT);
             failed_at = 0;
         }
     }
+    // Nothing before this wait touches the workspace header: the unordered
+    // low-latency mode zeroes it in the kernel this one waits for.
     pdl_wait();
+    if (lane == 0) {
+        if (failed_at == 0) set_device_error(a.err, MOE_DEVERR_COPY_TIMEOUT);
+        if (claimed == S) next_g = first_dynamic + atomicAdd(a.next_token, 1);
+    }
 
-    if (kLL) {
+    if (kMode == kLowLatency) {
         // counts[e*R + s]: the rank's tile totals for expert e
         const int n = E * rt.R;
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
@@ -449,7 +459,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
             for (int tau = rt.tile_off[s]; tau < rt.tile_off[s + 1]; ++tau) c += a.tile_hist[(long long)e * rt.ntiles + tau];
             a.counts[i] = c;
         }
-    } else {
+    } else if (kMode == kRagged) {
         // counts / offsets / expert_offsets from the scanned histogram
         const int n = E * rt.R;
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= n; i += gridDim.x * blockDim.x) {
@@ -482,20 +492,37 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
             if (lane < K) {
                 const long long i = g * K + lane;
                 e = __ldg(a.topk_idx + i);
-                const int lr = a.tok2row[i];
-                if (e >= 0 && e < E && lr >= 0) {
-                    const int tile = rt.tile_off[sidx] + (int)((i - item0) / kTileItems);
-                    if (kLL) {
-                        int base = (e * rt.R + sidx) * a.C;
-                        for (int tau = rt.tile_off[sidx]; tau < tile; ++tau)
-                            base += a.tile_hist[(long long)e * rt.ntiles + tau];
-                        row = base + lr;
+                if (kMode == kLowLatencyUnordered) {
+                    if (e >= 0 && e < E) {
+                        const int region = e * rt.R + sidx;
+                        const int slot = atomicAdd(a.counts + region, 1);
+                        // every B[s] <= C, so a region never overflows; the check keeps a
+                        // write inside the rectangle whatever the input
+                        row = (slot < a.C) ? region * a.C + slot : -1;
                     } else {
-                        row = a.scan[(long long)e * rt.ntiles + tile] + lr;
+                        set_device_error(a.err, MOE_DEVERR_EXPERT_RANGE);
                     }
-                    a.row2src[row] = (int32_t)i;
+                    if (row >= 0) {
+                        a.row2src[row] = (int32_t)i;
+                    } else {
+                        e = -1;
+                    }
                 } else {
-                    e = -1;
+                    const int lr = a.tok2row[i];
+                    if (e >= 0 && e < E && lr >= 0) {
+                        const int tile = rt.tile_off[sidx] + (int)((i - item0) / kTileItems);
+                        if (kMode == kLowLatency) {
+                            int base = (e * rt.R + sidx) * a.C;
+                            for (int tau = rt.tile_off[sidx]; tau < tile; ++tau)
+                                base += a.tile_hist[(long long)e * rt.ntiles + tau];
+                            row = base + lr;
+                        } else {
+                            row = a.scan[(long long)e * rt.ntiles + tile] + lr;
+                        }
+                        a.row2src[row] = (int32_t)i;
+                    } else {
+                        e = -1;
+                    }
                 }
                 a.tok2row[i] = row;
                 s_rows[warp][lane] = row;
@@ -645,13 +672,19 @@ static cudaError_t scatter_blocks_per_sm(const void *kfn, size_t smem, int *per_
 
 // Persistent launch of the scatter (one wave), with programmatic stream
 // serialization so that it stages its first rows while the previous kernel ends.
-static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, bool ll, cudaStream_t stream) {
+template <int kMode>
+static const void *scatter_fn(bool fp8) {
+    return fp8 ? (const void *)scatter_kernel<true, kMode> : (const void *)scatter_kernel<false, kMode>;
+}
+
+static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, int mode, cudaStream_t stream) {
     const long long T = a.T;
     const int H = a.H;
     cudaError_t ce;
     const size_t smem = scatter_stage_bytes(H, fp8) * MOE_SCATTER_STAGES * MOE_SCATTER_WARPS;
-    const void *kfn = fp8 ? (ll ? (const void *)scatter_kernel<true, true> : (const void *)scatter_kernel<true, false>)
-                          : (ll ? (const void *)scatter_kernel<false, true> : (const void *)scatter_kernel<false, false>);
+    const void *kfn = mode == kRagged       ? scatter_fn<kRagged>(fp8)
+                      : mode == kLowLatency ? scatter_fn<kLowLatency>(fp8)
+                                            : scatter_fn<kLowLatencyUnordered>(fp8);
     int per_sm = 0;
     if ((ce = scatter_blocks_per_sm(kfn, smem, &per_sm)) != cudaSuccess) return ce;
     if (per_sm < 1) per_sm = 1;
@@ -672,12 +705,8 @@ static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (fp8)
-        ce = ll ? cudaLaunchKernelEx(&cfg, scatter_kernel<true, true>, a, rt)
-                : cudaLaunchKernelEx(&cfg, scatter_kernel<true, false>, a, rt);
-    else
-        ce = ll ? cudaLaunchKernelEx(&cfg, scatter_kernel<false, true>, a, rt)
-                : cudaLaunchKernelEx(&cfg, scatter_kernel<false, false>, a, rt);
+    void *params[] = {&a, const_cast<RankTable *>(&rt)};
+    ce = cudaLaunchKernelExC(&cfg, kfn, params);
     if (ce != cudaSuccess) return ce;
     return cudaGetLastError();
 }
@@ -735,7 +764,7 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
     a.E = E;
     a.K = K;
     a.H = H;
-    return launch_scatter(a, rt, fp8, false, stream);
+    return launch_scatter(a, rt, fp8, kRagged, stream);
 }
 
 cudaError_t launch_dispatch_ll(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
@@ -769,8 +798,50 @@ cudaError_t launch_dispatch_ll(const void *x, const int32_t *topk_idx, const Ran
     a.K = K;
     a.H = H;
     a.C = C;
-    return launch_scatter(a, rt, fp8, true, stream);
+    return launch_scatter(a, rt, fp8, kLowLatency, stream);
 }
 
+
+// Zero the workspace header (error word, token counter) and the region counts
+// of the unordered low-latency dispatch; the scatter (launched with
+// programmatic stream serialization) stages its first rows meanwhile and
+// waits for this grid before it touches either.
+__global__ void zero_counts_kernel(int32_t *__restrict__ header, int32_t *__restrict__ counts, int n) {
+    pdl_launch_dependents();
+    const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+    if (tid < (int)(kWsHeader / 4)) header[tid] = 0;
+    for (int i = tid; i < n; i += gridDim.x * blockDim.x) counts[i] = 0;
+}
+
+cudaError_t launch_dispatch_ll_unordered(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K,
+                                         int H, int C, bool fp8, void *recv_x, float *recv_scale, int32_t *counts,
+                                         int32_t *tok2row, int32_t *row2src, void *workspace, cudaStream_t stream) {
+    const long long T = rt.rank_off[rt.R];
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    int32_t *err = reinterpret_cast<int32_t *>(ws);
+
+    cudaError_t ce;
+    const int n = E * rt.R;
+    const int zblocks = (n + 1023) / 1024 < 64 ? (n + 1023) / 1024 : 64;
+    zero_counts_kernel<<<zblocks, 1024, 0, stream>>>(err, counts, n);
+    if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
+
+    ScatterArgs a{};
+    a.x = static_cast<const __nv_bfloat16 *>(x);
+    a.topk_idx = topk_idx;
+    a.recv_x = recv_x;
+    a.recv_scale = recv_scale;
+    a.counts = counts;
+    a.tok2row = tok2row;
+    a.row2src = row2src;
+    a.err = err;
+    a.next_token = reinterpret_cast<int32_t *>(ws + 8);   // scatter token counter
+    a.T = (int)T;
+    a.E = E;
+    a.K = K;
+    a.H = H;
+    a.C = C;
+    return launch_scatter(a, rt, fp8, kLowLatencyUnordered, stream);
+}
 
 }  // namespace moe

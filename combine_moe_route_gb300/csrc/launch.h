@@ -31,6 +31,9 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
 cudaError_t launch_dispatch_ll(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
                                int C, bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *tok2row,
                                int32_t *row2src, void *workspace, cudaStream_t stream);
+cudaError_t launch_dispatch_ll_unordered(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K,
+                                         int H, int C, bool fp8, void *recv_x, float *recv_scale, int32_t *counts,
+                                         int32_t *tok2row, int32_t *row2src, void *workspace, cudaStream_t stream);
 cudaError_t launch_combine(const void *y, const int32_t *tok2row, const float *topk_w, int T, int K, int H,
                            bool out_f32, void *out, long long rows, cudaStream_t stream);
 cudaError_t launch_combine_push(const void *y, const int32_t *row2src, const int32_t *counts, int C, int H,

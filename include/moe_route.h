@@ -307,6 +307,37 @@ MOE_API moe_status moe_dispatch_ll(const void *x, const int32_t *topk_idx, int R
                                    void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * moe_dispatch_ll_unordered -- the low-latency dispatch with sender-side
+ * slots ([EPK] "Optimising for latency: send without asking": the sender
+ * alone writes its (source rank, expert) region, so it can number its own
+ * copies there without asking anyone).  A copy takes its slot by one atomic
+ * increment of its region's count, so no histogram or scan runs before the
+ * copies move; the call is two kernels (zero the counts, scatter).  Rows, counts
+ * and maps are those of moe_dispatch_ll up to the order of the rows inside
+ * each region, which is unspecified and may differ from call to call:
+ *   - counts[e*R + s] is exact (the number of rank s's copies routed to e);
+ *   - region (e, s) holds exactly those copies in rows (e*R + s)*C + [0, counts);
+ *   - tok2row and row2src are inverse maps over the filled rows;
+ *   - each filled row holds its token's bytes (and FP8 scales) exactly as
+ *     moe_dispatch_ll writes them.
+ * moe_combine_ll over these rows therefore gives bit-identical sums (it adds
+ * in the fixed order j through tok2row).  The sources fix the region of a copy
+ * but not its place inside the region; moe_dispatch_ll numbers the copies in
+ * token order, which needs the per-rank histogram first, and this entry lets
+ * the order fall out of the increments instead.
+ *
+ *   arguments  as moe_dispatch_ll, except that only the first 256 bytes of
+ *              the workspace are used (workspace_bytes >= 256).
+ * Errors: as moe_dispatch_ll.  T == 0 writes zeros to counts and launches no
+ * kernel.
+ */
+MOE_API moe_status moe_dispatch_ll_unordered(const void *x, const int32_t *topk_idx, int R, const int32_t *B,
+                                             int E, int K, int H, int C, moe_dtype recv_dtype,
+                                             void *recv_x, float *recv_scale, int32_t *counts,
+                                             int32_t *tok2row, int32_t *row2src,
+                                             void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
  * moe_combine_ll -- moe_combine over the low-latency rectangle: y is
  * [E*R*C, H] bf16 (expert outputs in moe_dispatch_ll's rows), tok2row is
  * moe_dispatch_ll's; indices outside [0, E*R*C) contribute nothing.  The sum,
