@@ -6,12 +6,14 @@
 // goes to K routed experts whose outputs are summed with weights.
 //
 // One warp per token.  Lane l holds logits e = l, l+32, l+64, ... in
-// registers as an order-preserving 32-bit image of each fp32 value, sorts
-// them once (a bitonic network on (key, expert) pairs) and keeps the sorted
-// list in shared memory.  K rounds of: warp-wide maximum of the lanes' list
-// heads by one redux.sync, then the smallest expert id among the lanes
-// holding that maximum by a second one; the owning lane pops its head.  A
-// round therefore costs O(1) per lane instead of a pass over E/32 keys.
+// registers as an order-preserving 32-bit image of each fp32 value.  The
+// K-th largest lane maximum tau (K rounds of redux.sync over the lane maxima)
+// is a lower bound of the row's K-th largest key, so the top K is among the
+// candidates key >= tau -- on random rows K plus a few.  The candidates are
+// compacted into shared memory and each one's output position is the number
+// of candidates ahead of it (larger key, or equal key and smaller id).  Rows
+// with more than kMaxCandidates candidates (many equal keys) instead take K
+// rounds of (lane best, redux.sync max of the key, redux.sync min of the id).
 // The weights are a softmax over the K winners, max-subtracted (the first
 // winner is the largest), exponentials summed in j order, one IEEE division.
 #include "launch.h"
@@ -30,33 +32,13 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
     return __uint_as_float(u);
 }
 
-// Descending bitonic sort of N (a power of two) values held in registers.
-template <int N>
-__device__ __forceinline__ void bitonic_sort_desc(unsigned long long (&c)[N]) {
-#pragma unroll
-    for (int size = 2; size <= N; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const bool desc = (i & size) == 0;   // direction of this bitonic run
-                    const unsigned long long a = c[i], b = c[j];
-                    const bool swap = desc ? (a < b) : (a > b);
-                    c[i] = swap ? b : a;
-                    c[j] = swap ? a : b;
-                }
-            }
-        }
-    }
-}
-
-template <int NPL>   // logits per lane: E <= 32 * NPL
 struct RouteShape {
-    static constexpr int kSlots = (NPL & (NPL - 1)) == 0 ? NPL : (NPL <= 16 ? 16 : 32);   // NPL padded to 2^n
-    static constexpr int kWarps = kSlots >= 32 ? 4 : 8;                                     // 32 KB list at most
+    static constexpr int kWarps = 8;   // tokens (warps) per block
 };
+
+// Candidates ranked in shared memory; a row with more candidates than this
+// (many equal keys) takes the K-round path instead.
+constexpr int kMaxCandidates = 64;
 
 // G > 1: group-limited routing (Perplexity, "Lower latency and higher
 // throughput with multi-node DeepSeek deployment", "MoE router": DeepSeek's
@@ -64,15 +46,15 @@ struct RouteShape {
 // form G contiguous groups; a group scores its largest logit; the M best
 // groups are kept (equal scores: smaller group id) and only their experts
 // stay eligible for the K rounds.
-template <int NPL>
-__global__ void __launch_bounds__(RouteShape<NPL>::kWarps * 32) route_topk_kernel(const float *__restrict__ logits,
+template <int NPL>   // logits per lane: E <= 32 * NPL
+__global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(const float *__restrict__ logits,
                                                                                   int T, int E, int K, int G, int M,
                                                                                   int32_t *__restrict__ topk_idx,
                                                                                   float *__restrict__ topk_w) {
-    constexpr int NS = RouteShape<NPL>::kSlots;
-    constexpr int kWarps = RouteShape<NPL>::kWarps;
+    constexpr int kWarps = RouteShape::kWarps;
     __shared__ uint32_t s_gmax[kWarps][32];
-    __shared__ unsigned long long s_list[kWarps][NS * 32];
+    __shared__ unsigned long long s_cand[kWarps][kMaxCandidates];
+    __shared__ unsigned long long s_win[kWarps][MOE_MAX_TOPK];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const long long g = (long long)blockIdx.x * kWarps + warp;
@@ -115,37 +97,85 @@ __global__ void __launch_bounds__(RouteShape<NPL>::kWarps * 32) route_topk_kerne
             if (!((kept >> ((lane + 32 * i) / gs)) & 1u)) avail &= ~(1u << i);
     }
 
-    // Each lane sorts its eligible candidates once, descending, as 64-bit
-    // (key, ~expert) composites -- on equal keys the smaller expert comes
-    // first -- and parks the sorted list in shared memory, interleaved by
-    // lane.  Then K rounds: every lane offers the head of its list; the warp
-    // keeps the largest key (redux.sync) and, among the lanes offering it, the
-    // smallest expert id (a second redux.sync); the winning lane's head moves
-    // one entry on.  Empty entries are 0 and never win (every real key is > 0).
-    unsigned long long c[NS];
+    // Threshold: tau = the K-th largest of the 32 lane maxima.  The K lanes
+    // with the largest maxima hold K keys >= tau, so the K-th largest key of
+    // the row is >= tau, and every member of the top K (ties included) is a
+    // candidate: an eligible key >= tau.  On random rows only a few keys
+    // beyond K pass.
+    uint32_t ek[NPL];   // eligible keys; 0 = not eligible (every real key is > 0)
+    uint32_t lmax = 0u;
 #pragma unroll
-    for (int i = 0; i < NS; ++i)
-        c[i] = (i < NPL && (avail & (1u << i)))
-                   ? ((unsigned long long)key[i] << 32) | (unsigned long long)(~(uint32_t)(lane + 32 * i))
-                   : 0ull;
-    bitonic_sort_desc<NS>(c);
-    unsigned long long *list = s_list[warp];
+    for (int i = 0; i < NPL; ++i) {
+        ek[i] = (avail & (1u << i)) ? key[i] : 0u;
+        lmax = max(lmax, ek[i]);
+    }
+    uint32_t tau = 0u;
+    for (int k = 0; k < K; ++k) {
+        const uint32_t top = __reduce_max_sync(0xffffffffu, lmax);
+        tau = top;
+        if (top == 0u) break;   // fewer than K lanes hold a key: every eligible key is a candidate
+        const uint32_t who = __reduce_min_sync(0xffffffffu, (lmax == top) ? (uint32_t)lane : 32u);
+        if ((uint32_t)lane == who) lmax = 0u;
+    }
+    uint32_t cm = 0u;   // bit i: slot i is a candidate
 #pragma unroll
-    for (int i = 0; i < NS; ++i) list[i * 32 + lane] = c[i];
-    __syncwarp();
-    int head = 0;
+    for (int i = 0; i < NPL; ++i)
+        if (ek[i] != 0u && ek[i] >= tau) cm |= 1u << i;
+    const int cnt = __popc(cm);
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const int n = __shfl_sync(0xffffffffu, incl, 31);
+
     int my_e = 0;
     uint32_t my_key = 0;
-    for (int k = 0; k < K; ++k) {
-        const unsigned long long h = (head < NS) ? list[head * 32 + lane] : 0ull;
-        const uint32_t hk = (uint32_t)(h >> 32);
-        const uint32_t kmax = __reduce_max_sync(0xffffffffu, hk);
-        const uint32_t cand = (hk == kmax && hk != 0u) ? ~(uint32_t)h : 0xffffffffu;
-        const uint32_t e_win = __reduce_min_sync(0xffffffffu, cand);
-        if ((int)(e_win & 31u) == lane) ++head;
-        if (lane == k) {
-            my_e = (int)e_win;
-            my_key = kmax;
+    if (n <= kMaxCandidates) {
+        // rank each candidate by the 64-bit (key, ~expert) composite: a larger
+        // composite is a larger key or, on equal keys, a smaller expert id
+        unsigned long long *cand = s_cand[warp];
+        int pos = incl - cnt;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i)
+            if (cm & (1u << i)) cand[pos++] = ((unsigned long long)ek[i] << 32) | (unsigned long long)(~(uint32_t)(lane + 32 * i));
+        __syncwarp();
+        for (int c = lane; c < n; c += 32) {
+            const unsigned long long me = cand[c];
+            int r = 0;
+            for (int m = 0; m < n; ++m) r += (cand[m] > me) ? 1 : 0;
+            if (r < K) s_win[warp][r] = me;
+        }
+        __syncwarp();
+        if (lane < K) {
+            const unsigned long long wv = s_win[warp][lane];
+            my_key = (uint32_t)(wv >> 32);
+            my_e = (int)~(uint32_t)wv;
+        }
+    } else {
+        // many equal keys: K rounds of (each lane's best remaining key, the
+        // warp's largest by redux.sync, the smallest expert id among the lanes
+        // holding it by a second redux.sync; the owner retires it)
+        for (int k = 0; k < K; ++k) {
+            uint32_t bk = 0u;
+            int bi = -1;
+#pragma unroll
+            for (int i = 0; i < NPL; ++i)
+                if (ek[i] > bk) {
+                    bk = ek[i];
+                    bi = i;
+                }
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t cand = (bi >= 0 && bk == kmax) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+            const uint32_t e_win = __reduce_min_sync(0xffffffffu, cand);
+#pragma unroll
+            for (int i = 0; i < NPL; ++i)
+                if ((uint32_t)(lane + 32 * i) == e_win) ek[i] = 0u;
+            if (lane == k) {
+                my_e = (int)e_win;
+                my_key = kmax;
+            }
         }
     }
 
@@ -164,8 +194,8 @@ __global__ void __launch_bounds__(RouteShape<NPL>::kWarps * 32) route_topk_kerne
 cudaError_t launch_route_topk(const float *logits, int T, int E, int K, int G, int M, int32_t *topk_idx,
                               float *topk_w, cudaStream_t stream) {
 #define MOE_ROUTE_LAUNCH(NPL)                                                                       \
-    route_topk_kernel<NPL><<<(unsigned)((T + RouteShape<NPL>::kWarps - 1) / RouteShape<NPL>::kWarps), \
-                             RouteShape<NPL>::kWarps * 32, 0, stream>>>(logits, T, E, K, G, M, topk_idx, topk_w)
+    route_topk_kernel<NPL><<<(unsigned)((T + RouteShape::kWarps - 1) / RouteShape::kWarps), RouteShape::kWarps * 32, \
+                             0, stream>>>(logits, T, E, K, G, M, topk_idx, topk_w)
     if (E <= 32)
         MOE_ROUTE_LAUNCH(1);
     else if (E <= 64)

@@ -176,6 +176,33 @@ def test_route_grouped(E, K, G, M, T, gpu, oracle):
         assert torch.equal(p_idx, idx) and torch.equal(p_w, w)
 
 
+@pytest.mark.parametrize("E,K,T", [(1, 1, 70), (5, 3, 300), (31, 7, 500), (33, 8, 500), (100, 32, 400),
+                                   (256, 8, 3000), (384, 8, 1200), (1000, 16, 300), (1024, 32, 256)])
+def test_route_plain_shapes(E, K, T, gpu, oracle):
+    """Plain top-K on rows of every kind: random; rounded (many exact ties, more candidates than
+    the shared-memory ranking takes); constant; +0 and -0 mixed; and a row whose K-th and
+    (K+1)-th keys tie across lanes."""
+    b = _binding()
+    rng = np.random.default_rng(E * 7 + K)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    q = T // 5
+    logits[q:2 * q] = np.round(logits[q:2 * q])
+    logits[2 * q:2 * q + 3] = 1.5
+    logits[2 * q + 3] = np.where(rng.random(E) < 0.5, 0.0, -0.0).astype(np.float32)
+    if E > K:
+        row = rng.standard_normal(E).astype(np.float32)
+        top = np.sort(row)[::-1]
+        row[row == top[K]] = top[K - 1]                    # the K-th and (K+1)-th keys now tie
+        logits[2 * q + 4] = row
+    lg = torch.from_numpy(logits).to(gpu)
+    idx, w = b.route_topk(lg, K)
+    torch.cuda.synchronize()
+    o_idx, o_w = oracle.route_topk(logits, K)
+    assert np.array_equal(i32(idx), o_idx)
+    sel = np.take_along_axis(logits, o_idx, axis=1)
+    assert np.all(np.abs(f32(w).astype(np.float64) - o_w) <= weight_tolerance(o_w, sel, K))
+
+
 # ---------------------------------------------------------------------------
 # random small shapes, ragged tails, edge cases
 # ---------------------------------------------------------------------------
