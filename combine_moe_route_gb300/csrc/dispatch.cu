@@ -29,9 +29,9 @@
 //     grouped by a ballot per bit of the expert id and their leader adds the
 //     group size with one shared-memory atomic, whose return value plus the
 //     lane's position in the group is the item's rank among equal experts so
-//     far.  The warps'
-//     histograms are then combined in warp order, giving every item a stable
-//     rank inside (expert, tile) and every tile its per-expert total.
+//     far.  The warps' histograms are then combined in warp order, giving
+//     every item a stable rank inside (expert, tile) and every tile its
+//     per-expert total.
 //  2. exclusive scan over the histogram laid out expert-major, tile-minor
 //     (e * ntiles + tile), one pass with decoupled lookback.  Because tiles
 //     are rank-major and ranks hold consecutive tokens, this order is exactly
@@ -43,6 +43,8 @@
 // The low-latency layout (lehuy.net, same article, "Optimising for latency:
 // send without asking") skips the scan: its rows are a static formula over a
 // fixed region per (expert, source rank), so it runs kernels 1 and 3 only.
+// Its unordered form lets each copy take its slot in the region by an atomic
+// increment, and runs a zeroing kernel and kernel 3 only.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
