@@ -28,6 +28,25 @@ namespace moe {
 constexpr int kCombineThreads = 128;
 constexpr int kCombineBatch = 8;   // row loads in flight per chunk
 
+// bf16 pair (low half = first element) -> two fp32, exactly (bf16 is the high
+// half of an fp32).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // round to nearest even
+    return (uint32_t)__bfloat16_as_ushort(h.x) | ((uint32_t)__bfloat16_as_ushort(h.y) << 16);
+}
+
+// acc[0..7] += w * (8 bf16 channels of v), in channel order.
+__device__ __forceinline__ void fma_row(float (&acc)[8], float w, const uint4 v) {
+    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        acc[2 * k] = __fmaf_rn(w, bf16_lo(q[k]), acc[2 * k]);
+        acc[2 * k + 1] = __fmaf_rn(w, bf16_hi(q[k]), acc[2 * k + 1]);
+    }
+}
+
 // tok2row == nullptr reads row g*K + j (the layout a push-style return leaves
 // on the origin rank); rows = number of rows of y (indices outside are skipped).
 template <bool kOutF32>
@@ -63,16 +82,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __nv_bfl
 #pragma unroll
                 for (int jj = 0; jj < kCombineBatch; ++jj) {
                     const int j = j0 + jj;
-                    if (j < K && s_row[j] >= 0) {
-                        const float w = s_w[j];
-                        const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&v[jj]);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float2 f = __bfloat1622float2(h2[k]);
-                            acc[2 * k] = __fmaf_rn(w, f.x, acc[2 * k]);
-                            acc[2 * k + 1] = __fmaf_rn(w, f.y, acc[2 * k + 1]);
-                        }
-                    }
+                    if (j < K && s_row[j] >= 0) fma_row(acc, s_w[j], v[jj]);
                 }
             }
             if (kOutF32) {
@@ -82,11 +92,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __nv_bfl
                 st_v4(o + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]), __float_as_uint(acc[6]),
                                         __float_as_uint(acc[7])));
             } else {
-                uint4 pk;
-                __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) p2[k] = __floats2bfloat162_rn(acc[2 * k], acc[2 * k + 1]);
-                st_v4(static_cast<__nv_bfloat16 *>(out) + (size_t)g * H + (size_t)c * 8, pk);
+                st_v4(static_cast<__nv_bfloat16 *>(out) + (size_t)g * H + (size_t)c * 8,
+                      make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                                 pack_bf16x2(acc[6], acc[7])));
             }
         }
     }
