@@ -48,6 +48,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "launch.h"
@@ -617,17 +618,20 @@ DispatchPlan plan_dispatch(int E, int ntiles) {
 
 int max_tiles(int R, int K, long long T) { return (int)((T * K + kTileItems - 1) / kTileItems) + R; }
 
+// SM count of the current device, asked once per device (host threads may
+// race to fill an entry; they all store the same value).
 static int sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    if (cached[dev] == 0) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n > 0 ? n : 1;
+        if (n < 1) n = 1;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 int device_sm_count() { return sm_count(); }
