@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -400,6 +401,28 @@ class OracleLayer:
         return t2 - t0
 
 
+def pct(ms: list) -> list:
+    """[p10, p90] of a list of millisecond timings, in µs."""
+    q = sorted(ms)
+    at = lambda f: q[min(len(q) - 1, int(round(f * (len(q) - 1))))] * 1e3
+    return [at(0.10), at(0.90)]
+
+
+def host_cpu() -> dict:
+    """The host's logical CPU count and model name (from /proc/cpuinfo where it has one)."""
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "model": model}
+
+
 def cpu_baseline(workload: str, T_full: int):
     from combine_moe_route_gb300 import workloads as wl
     w = wl.WORKLOADS[workload]
@@ -414,7 +437,7 @@ def cpu_baseline(workload: str, T_full: int):
             break
     T_s = inp["T"]
     per_layer_us = statistics.median(times) * 1e6 * (T_full / T_s)
-    return {"value": per_layer_us, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": per_layer_us, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
             "sample": f"{workload} with {tpr} tokens/rank (T={T_s} of {T_full}); median of {len(times)} "
                       "runs of oracle dispatch + combine, scaled by T_full/T_sample; single-threaded C"}
 
@@ -442,7 +465,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": bench_config(w, T_full, "CPU oracle"),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
                          "sample": f"{args.workload} with {tpr} tokens/rank per step (T={inp['T']} of {T_full}), "
                                    "oracle dispatch + combine scaled by T_full/T_sample; single-threaded C"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -548,6 +571,20 @@ def run_ours(args, world, rank, local):
     dc_us = statistics.mean(a + c for a, c in zip(disp_ms, comb_ms)) * 1e3
     dc_us_max = max_over_ranks(dc_us, world, dev)
     step_ms_max = max_over_ranks(total_ms / args.steps, world, dev)
+
+    # the same calls with the L2 left warm (no flush between them), outside the timed region
+    uev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(20)]
+    for e in uev:
+        e[0].record(stream)
+        b.dispatch(x, idx, B, E, fp8=w.fp8, out=d)
+        e[1].record(stream)
+        e[2].record(stream)
+        b.combine(y, d.tok2row, wts, out=out)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    unflushed = {"dispatch": statistics.mean(e[0].elapsed_time(e[1]) for e in uev[2:]) * 1e3,
+                 "combine": statistics.mean(e[2].elapsed_time(e[3]) for e in uev[2:]) * 1e3,
+                 "note": "back-to-back calls without an L2 flush; the expert stand-in does not run between them"}
 
     # end to end through the public API: pinned host inputs -> device -> layer -> pinned host output.
     # Serial: one layer after another on one stream.  Pipelined (HostLayerPipeline): the input copy
@@ -666,6 +703,8 @@ def run_ours(args, world, rank, local):
                 "dispatch_frac_of_measured": d_gbs / peak, "combine_frac_of_measured": c_gbs / peak,
                 "route_GBps": route_bytes(T, E, K) / (r_us * 1e-6) / 1e9},
         "p50_us": {"dispatch": statistics.median(disp_ms) * 1e3, "combine": statistics.median(comb_ms) * 1e3},
+        "p10_p90_us": {"dispatch": pct(disp_ms), "combine": pct(comb_ms)},
+        "unflushed_us": unflushed,
         "e2e": {"value": replica_value(e2e_us, world), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_h.numel() * 2 + lg_h.numel() * 4),
                 "d2h_bytes_per_step": int(out_h.numel() * 2),
