@@ -11,25 +11,37 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "launch.h"
 
 namespace moe {
 
 constexpr int kExpertThreads = 256;
+#ifndef MOE_EXPERT_UNROLL
+#define MOE_EXPERT_UNROLL 2   // 16-byte chunks per lane in flight at once
+#endif
+constexpr int kU = MOE_EXPERT_UNROLL;
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // round to nearest even
+    return (uint32_t)__bfloat16_as_ushort(h.x) | ((uint32_t)__bfloat16_as_ushort(h.y) << 16);
+}
+
+// 8 fp32 values times s_e, rounded to bf16 and packed (first value in the low half).
 __device__ __forceinline__ uint4 scale_to_bf16x8(const float *f, float se) {
-    uint4 pk;
-    __nv_bfloat162 *p2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) p2[k] = __floats2bfloat162_rn(__fmul_rn(f[2 * k], se), __fmul_rn(f[2 * k + 1], se));
-    return pk;
+    return make_uint4(pack_bf16x2(__fmul_rn(f[0], se), __fmul_rn(f[1], se)),
+                      pack_bf16x2(__fmul_rn(f[2], se), __fmul_rn(f[3], se)),
+                      pack_bf16x2(__fmul_rn(f[4], se), __fmul_rn(f[5], se)),
+                      pack_bf16x2(__fmul_rn(f[6], se), __fmul_rn(f[7], se)));
 }
 
 // One warp per row (rows warp-strided over a persistent grid).  Lane 0 finds
 // the row's expert by binary search over expert_offsets in shared memory.
-// FP8: a lane takes 16 e4m3 values (16 bytes) at a time, decodes them exactly
+// FP8: a lane takes 16 e4m3 values (16 bytes) per chunk, decodes them exactly
 // through half precision, multiplies by the block scale and by s_e, and
-// writes 32 bytes of bf16.  bf16: 8 values (16 bytes) in, 16 bytes out.
+// writes 32 bytes of bf16.  bf16: 8 values (16 bytes) in, 16 bytes out.  Each
+// lane issues the loads of kU chunks before converting any of them.
 template <bool kFp8>
 __global__ void __launch_bounds__(kExpertThreads) expert_scale_kernel(const void *__restrict__ recv,
                                                                       const float *__restrict__ recv_scale,
@@ -58,47 +70,93 @@ __global__ void __launch_bounds__(kExpertThreads) expert_scale_kernel(const void
         if (kFp8) {
             const unsigned char *qr = static_cast<const unsigned char *>(recv) + (size_t)row * H;
             const float *sr = recv_scale + (size_t)row * nblk;
-            for (int c = lane; c < H / 16; c += 32) {
-                const uint4 q = ld_stream_v4(qr + (size_t)c * 16);
-                const float sc = __ldg(sr + (c >> 3));   // 8 chunks of 16 per 128-channel block
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-                float f[16];
+            const int nc = H / 16;
+            for (int c0 = lane; c0 < nc; c0 += 32 * kU) {
+                uint4 q[kU];
+                float sc[kU];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[k >> 1] >> (16 * (k & 1))) & 0xffffu);
-                    const float2 fl = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
-                    f[2 * k] = __fmul_rn(fl.x, sc);
-                    f[2 * k + 1] = __fmul_rn(fl.y, sc);
+                for (int u = 0; u < kU; ++u) {
+                    const int c = c0 + 32 * u;
+                    q[u] = (c < nc) ? ld_stream_v4(qr + (size_t)c * 16) : make_uint4(0u, 0u, 0u, 0u);
+                    sc[u] = (c < nc) ? __ldg(sr + (c >> 3)) : 0.0f;   // 8 chunks of 16 per 128-channel block
                 }
-                st_v4(yr + (size_t)c * 16, scale_to_bf16x8(f, se));
-                st_v4(yr + (size_t)c * 16 + 8, scale_to_bf16x8(f + 8, se));
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c >= nc) break;
+                    const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+                    float f[16];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const __nv_fp8x2_storage_t pair =
+                            (__nv_fp8x2_storage_t)((w[k >> 1] >> (16 * (k & 1))) & 0xffffu);
+                        const float2 fl = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
+                        f[2 * k] = __fmul_rn(fl.x, sc[u]);
+                        f[2 * k + 1] = __fmul_rn(fl.y, sc[u]);
+                    }
+                    st_v4(yr + (size_t)c * 16, scale_to_bf16x8(f, se));
+                    st_v4(yr + (size_t)c * 16 + 8, scale_to_bf16x8(f + 8, se));
+                }
             }
         } else {
             const __nv_bfloat16 *xr = static_cast<const __nv_bfloat16 *>(recv) + (size_t)row * H;
-            for (int c = lane; c < H / 8; c += 32) {
-                const uint4 u = ld_stream_v4(xr + (size_t)c * 8);
-                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
-                float f[8];
+            const int nc = H / 8;
+            for (int c0 = lane; c0 < nc; c0 += 32 * kU) {
+                uint4 v[kU];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 t = __bfloat1622float2(h2[k]);
-                    f[2 * k] = t.x;
-                    f[2 * k + 1] = t.y;
+                for (int u = 0; u < kU; ++u) {
+                    const int c = c0 + 32 * u;
+                    v[u] = (c < nc) ? ld_stream_v4(xr + (size_t)c * 8) : make_uint4(0u, 0u, 0u, 0u);
                 }
-                st_v4(yr + (size_t)c * 8, scale_to_bf16x8(f, se));
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c >= nc) break;
+                    // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32
+                    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                    float f[8];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        f[2 * k] = __uint_as_float(w[k] << 16);
+                        f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+                    }
+                    st_v4(yr + (size_t)c * 8, scale_to_bf16x8(f, se));
+                }
             }
         }
     }
 }
 
+// Blocks per SM that fit, asked once per kernel variant and device; the grid
+// is one full wave of them (a partial second wave would idle most SMs).
+template <bool kFp8>
+static int expert_blocks_per_sm() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        // the shared-memory need ((E+1)*4 bytes) is far below the per-SM limit at
+        // every E this library takes, so the answer at the largest E serves all
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, expert_scale_kernel<kFp8>, kExpertThreads,
+                                                          (size_t)(MOE_MAX_EXPERTS + 1) * 4) != cudaSuccess ||
+            n < 1)
+            n = 1;
+        cached[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 cudaError_t launch_expert_scale(const void *recv, const float *recv_scale, bool fp8, const int32_t *expert_offsets,
                                 int E, int H, int rows, int identity, void *y, cudaStream_t stream) {
     const int warps = kExpertThreads / 32;
+    const size_t smem = (size_t)(E + 1) * 4;
     long long grid = ((long long)rows + warps - 1) / warps;
-    const long long cap = (long long)device_sm_count() * 8;
+    const long long cap =
+        (long long)device_sm_count() * (fp8 ? expert_blocks_per_sm<true>() : expert_blocks_per_sm<false>());
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    const size_t smem = (size_t)(E + 1) * 4;
     __nv_bfloat16 *yb = static_cast<__nv_bfloat16 *>(y);
     if (fp8)
         expert_scale_kernel<true><<<(unsigned)grid, kExpertThreads, smem, stream>>>(recv, recv_scale, expert_offsets, E,
