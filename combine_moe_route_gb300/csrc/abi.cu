@@ -145,28 +145,48 @@ moe_status moe_combine(const void *y, const int32_t *tok2row, const float *topk_
                                            (long long)T * K, (cudaStream_t)stream));
 }
 
-moe_status moe_dispatch_ll(const void *x, const int32_t *topk_idx, int R, const int32_t *B, int E, int K, int H, int C,
-                           moe_dtype recv_dtype, void *recv_x, float *recv_scale, int32_t *counts, int32_t *tok2row,
-                           int32_t *row2src, void *workspace, size_t workspace_bytes, moe_stream_t stream) {
+// Checks shared by the two low-latency dispatch entries.  On MOE_OK with
+// launch = true the call may go ahead with rt and fp8 filled; otherwise the
+// returned status is the call's result (T == 0 has zeroed counts and returns
+// MOE_OK with launch = false).  The ordered form needs the full dispatch
+// workspace (histogram tiles), the unordered one only the header.
+static moe_status check_dispatch_ll(bool ordered, const void *x, const int32_t *topk_idx, int R, const int32_t *B,
+                                    int E, int K, int H, int C, moe_dtype recv_dtype, void *recv_x,
+                                    float *recv_scale, int32_t *counts, int32_t *tok2row, int32_t *row2src,
+                                    void *workspace, size_t workspace_bytes, cudaStream_t st, moe::RankTable &rt,
+                                    bool &fp8, bool &launch) {
+    launch = false;
     if (R < 1 || R > MOE_MAX_RANKS || !B || !topk_shape_ok(E, K) || E % R != 0) return MOE_ERR_INVALID_ARG;
     if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0) return MOE_ERR_INVALID_ARG;
     if (recv_dtype != MOE_DTYPE_BF16 && recv_dtype != MOE_DTYPE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
-    const bool fp8 = recv_dtype == MOE_DTYPE_FP8_E4M3;
+    fp8 = recv_dtype == MOE_DTYPE_FP8_E4M3;
     if (fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
     if (C < 1 || (long long)E * R * C >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
-    moe::RankTable rt;
     long long T = 0;
     if (!build_rank_table(R, B, K, rt, T)) return MOE_ERR_INVALID_ARG;
     for (int s = 0; s < R; ++s)
         if (B[s] > C) return MOE_ERR_INVALID_ARG;   // the chunk cap bounds every region
     if (!counts) return MOE_ERR_INVALID_ARG;
-    cudaStream_t st = (cudaStream_t)stream;
     if (T == 0) return cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E * R, st));
     if (!x || !topk_idx || !recv_x || !tok2row || !row2src || (fp8 && !recv_scale)) return MOE_ERR_INVALID_ARG;
     if (!workspace) return MOE_ERR_WORKSPACE;
-    if (workspace_bytes < moe::plan_dispatch(E, rt.ntiles).total) return MOE_ERR_WORKSPACE;
+    const size_t need = ordered ? moe::plan_dispatch(E, rt.ntiles).total : moe::kWsHeader;
+    if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
     if (!aligned16(x) || !aligned16(recv_x) || !aligned16(workspace) || (fp8 && !aligned16(recv_scale)))
         return MOE_ERR_UNSUPPORTED;
+    launch = true;
+    return MOE_OK;
+}
+
+moe_status moe_dispatch_ll(const void *x, const int32_t *topk_idx, int R, const int32_t *B, int E, int K, int H, int C,
+                           moe_dtype recv_dtype, void *recv_x, float *recv_scale, int32_t *counts, int32_t *tok2row,
+                           int32_t *row2src, void *workspace, size_t workspace_bytes, moe_stream_t stream) {
+    const cudaStream_t st = (cudaStream_t)stream;
+    moe::RankTable rt;
+    bool fp8 = false, launch = false;
+    const moe_status v = check_dispatch_ll(true, x, topk_idx, R, B, E, K, H, C, recv_dtype, recv_x, recv_scale, counts,
+                                           tok2row, row2src, workspace, workspace_bytes, st, rt, fp8, launch);
+    if (v != MOE_OK || !launch) return v;
     return cuda_status(moe::launch_dispatch_ll(x, topk_idx, rt, E, K, H, C, fp8, recv_x, fp8 ? recv_scale : nullptr,
                                                counts, tok2row, row2src, workspace, st));
 }
@@ -175,25 +195,12 @@ moe_status moe_dispatch_ll_unordered(const void *x, const int32_t *topk_idx, int
                                      int H, int C, moe_dtype recv_dtype, void *recv_x, float *recv_scale,
                                      int32_t *counts, int32_t *tok2row, int32_t *row2src, void *workspace,
                                      size_t workspace_bytes, moe_stream_t stream) {
-    if (R < 1 || R > MOE_MAX_RANKS || !B || !topk_shape_ok(E, K) || E % R != 0) return MOE_ERR_INVALID_ARG;
-    if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0) return MOE_ERR_INVALID_ARG;
-    if (recv_dtype != MOE_DTYPE_BF16 && recv_dtype != MOE_DTYPE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
-    const bool fp8 = recv_dtype == MOE_DTYPE_FP8_E4M3;
-    if (fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
-    if (C < 1 || (long long)E * R * C >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+    const cudaStream_t st = (cudaStream_t)stream;
     moe::RankTable rt;
-    long long T = 0;
-    if (!build_rank_table(R, B, K, rt, T)) return MOE_ERR_INVALID_ARG;
-    for (int s = 0; s < R; ++s)
-        if (B[s] > C) return MOE_ERR_INVALID_ARG;   // the chunk cap bounds every region
-    if (!counts) return MOE_ERR_INVALID_ARG;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (T == 0) return cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E * R, st));
-    if (!x || !topk_idx || !recv_x || !tok2row || !row2src || (fp8 && !recv_scale)) return MOE_ERR_INVALID_ARG;
-    if (!workspace) return MOE_ERR_WORKSPACE;
-    if (workspace_bytes < moe::kWsHeader) return MOE_ERR_WORKSPACE;
-    if (!aligned16(x) || !aligned16(recv_x) || !aligned16(workspace) || (fp8 && !aligned16(recv_scale)))
-        return MOE_ERR_UNSUPPORTED;
+    bool fp8 = false, launch = false;
+    const moe_status v = check_dispatch_ll(false, x, topk_idx, R, B, E, K, H, C, recv_dtype, recv_x, recv_scale,
+                                           counts, tok2row, row2src, workspace, workspace_bytes, st, rt, fp8, launch);
+    if (v != MOE_OK || !launch) return v;
     return cuda_status(moe::launch_dispatch_ll_unordered(x, topk_idx, rt, E, K, H, C, fp8, recv_x,
                                                          fp8 ? recv_scale : nullptr, counts, tok2row, row2src,
                                                          workspace, st));
