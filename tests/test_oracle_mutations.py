@@ -109,6 +109,26 @@ MUTATIONS = [
      "int64_t row = ((int64_t)e * R + s) * C + slot;",
      "int64_t row = ((int64_t)s * E + e) * C + slot;",
      [P.test_ll_layout_is_the_ragged_layout_in_fixed_regions]),
+    ("group selection keeps the lowest-scoring groups",
+     "if (best < 0 || gscore[q] > gscore[best]) best = q;",
+     "if (best < 0 || gscore[q] < gscore[best]) best = q;",
+     [P.test_grouped_route_matches_library_sort]),
+    ("equal group scores go to the higher group id",
+     "if (best < 0 || gscore[q] > gscore[best]) best = q;",
+     "if (best < 0 || gscore[q] >= gscore[best]) best = q;",
+     [P.test_grouped_route_matches_library_sort]),
+    ("push return drops the last row of each region",
+     "for (int slot = 0; slot < counts[e * R + s]; ++slot) {",
+     "for (int slot = 0; slot + 1 < counts[e * R + s]; ++slot) {",
+     [P.test_ll_push_then_reduce_equals_gather]),
+    ("route weights not normalised",
+     "topk_w[(size_t)g * K + j] = (float)(ex[j] / sum);",
+     "topk_w[(size_t)g * K + j] = (float)(ex[j]);",
+     [P.test_route_weights_softmax]),
+    ("bf16 truncates instead of rounding",
+     "upper += 1u;                                 /* may carry into inf: correct */",
+     "upper += 0u;",
+     [F.test_bf16_rne_matches_library_cast, F.test_bf16_rne_ties_and_specials]),
     ("partial sums returned without their bf16 rounding",
      "acc = acc + oracle_f32_from_bf16(wire);",
      "acc = acc + part;",
