@@ -21,10 +21,12 @@
 namespace moe {
 
 // fp32 -> uint32 with the same order (+0 and -0 map to the same value).
+// Adding +0 turns -0 into +0 and leaves every other value unchanged (round to
+// nearest, denormals kept); then negative values have all bits flipped and
+// non-negative ones their sign bit set.
 __device__ __forceinline__ uint32_t ordered_key(float v) {
-    uint32_t u = __float_as_uint(v);
-    if (u == 0x80000000u) u = 0u;   // -0 == +0
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
+    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
 
 __device__ __forceinline__ float key_to_float(uint32_t k) {
