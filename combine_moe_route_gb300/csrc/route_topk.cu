@@ -77,15 +77,40 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
     }
 
     if (G > 1) {   // keep the M best groups; the experts of the others leave the race
-        uint32_t *gm = s_gmax[warp];
         const int gs = E / G;
-        if (lane < G) gm[lane] = 0u;
-        __syncwarp();
+        // group of slot i, when every slot lies inside one group (group size a
+        // multiple of 32): slots 0..spg-1 are group 0, and so on
+        const bool whole_slots = (gs & 31) == 0;
+        int slot_group[NPL];
+        uint32_t gkey = 0u;   // lane q < G: the largest key of group q (every real key is > 0)
+        if (whole_slots) {
+            const int spg = gs >> 5;
+            int q = 0, c = 0;
 #pragma unroll
-        for (int i = 0; i < NPL; ++i)
-            if (avail & (1u << i)) atomicMax(&gm[(lane + 32 * i) / gs], key[i]);
-        __syncwarp();
-        const uint32_t gkey = (lane < G) ? gm[lane] : 0u;   // every real group's key is > 0
+            for (int i = 0; i < NPL; ++i) {
+                slot_group[i] = q;
+                if (++c == spg) {
+                    c = 0;
+                    ++q;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+                const uint32_t m = __reduce_max_sync(0xffffffffu, (avail & (1u << i)) ? key[i] : 0u);
+                if (lane == slot_group[i]) gkey = max(gkey, m);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) slot_group[i] = (lane + 32 * i) / gs;
+            uint32_t *gm = s_gmax[warp];
+            if (lane < G) gm[lane] = 0u;
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < NPL; ++i)
+                if (avail & (1u << i)) atomicMax(&gm[slot_group[i]], key[i]);
+            __syncwarp();
+            if (lane < G) gkey = gm[lane];
+        }
         bool open = lane < G;
         uint32_t kept = 0u;
         for (int r = 0; r < M; ++r) {
@@ -96,7 +121,7 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
         }
 #pragma unroll
         for (int i = 0; i < NPL; ++i)
-            if (!((kept >> ((lane + 32 * i) / gs)) & 1u)) avail &= ~(1u << i);
+            if (slot_group[i] >= 32 || !((kept >> slot_group[i]) & 1u)) avail &= ~(1u << i);
     }
 
     // Threshold: tau = the K-th largest of the 32 lane maxima.  The K lanes
