@@ -169,3 +169,12 @@ def test_route_grouped_validation(lib):
     assert f(FAKE, 4, 64, 9, 8, 1, FAKE, FAKE, None) == INVALID        # K > kept experts (8)
     assert f(None, 4, 256, 8, 8, 4, FAKE, FAKE, None) == INVALID
     assert f(None, 0, 256, 8, 8, 4, None, None, None) == OK
+
+
+def test_plain_c_consumer_compiles_and_links(lib, tmp_path):
+    """The C ABI needs nothing but its header and the CUDA runtime: a plain C11 program
+    (tests/c_abi/roundtrip.c) compiles without warnings and links against the library."""
+    import _c_abi
+    from combine_moe_route_gb300 import build
+    exe = _c_abi.compile_roundtrip(build.library_path(), str(tmp_path))
+    assert os.path.exists(exe)
