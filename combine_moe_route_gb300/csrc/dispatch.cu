@@ -72,14 +72,25 @@ namespace moe {
 // --------------------------------------------------------------------------
 // 1. tile histogram + stable in-tile ranks
 // --------------------------------------------------------------------------
-// local_rank (aliases the tok2row output): in-tile rank of each item, or -1.
+// local_rank (aliases the tok2row output): in-tile rank of each item, or -1
+// (an expert id out of range; the scatter, which reads every id again,
+// reports it).  Block 0 also clears the call's workspace header (error word,
+// scan ticket, scatter token counter) and the lookback status words: nothing
+// reads or writes them before this grid has completed, so no memset has to
+// run ahead of this kernel.
 __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *__restrict__ topk_idx, int E, int K,
                                                                  const __grid_constant__ RankTable rt,
                                                                  int32_t *__restrict__ tile_hist,
                                                                  int32_t *__restrict__ local_rank,
-                                                                 int32_t *__restrict__ err) {
+                                                                 int32_t *__restrict__ header,
+                                                                 unsigned long long *__restrict__ status,
+                                                                 int nstatus) {
     extern __shared__ int32_t hist[];   // [kHistWarps][E]
     pdl_launch_dependents();            // the scan may launch; it waits for this grid's writes
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < (int)(kWsHeader / 4); i += blockDim.x) header[i] = 0;
+        for (int i = threadIdx.x; i < nstatus; i += blockDim.x) status[i] = 0ull;
+    }
     const int tile = blockIdx.x;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -98,7 +109,6 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
     const int ebits = (E > 1) ? 32 - __clz(E - 1) : 0;   // bits of the largest expert id
     int e_reg[kItemsPerThread];
     int r_reg[kItemsPerThread];
-    int bad = 0;
     // all of this thread's item loads first, so they are in flight together
 #pragma unroll
     for (int step = 0; step < kItemsPerThread; ++step) {
@@ -109,10 +119,7 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
     for (int step = 0; step < kItemsPerThread; ++step) {
         const long long i = lo + warp * kItemsPerWarp + step * 32 + lane;
         int e = e_reg[step];
-        if (i < hi && (e < 0 || e >= E)) {
-            bad = 1;
-            e = -1;
-        }
+        if (e >= E) e = -1;   // out of range: no rank (the scatter reports it)
         // lanes holding the same expert: one ballot per bit of the expert id
         // (a multi-split; its cost does not grow with the number of distinct
         // experts in the warp, unlike a match instruction)
@@ -133,7 +140,6 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
         r_reg[step] = (e >= 0) ? base + __popc(peers & lanemask_lt) : -1;
         __syncwarp();
     }
-    if (bad) set_device_error(err, MOE_DEVERR_EXPERT_RANGE);
     __syncthreads();
 
     // combine the warps' histograms in warp order: hist[w][e] becomes the
@@ -194,8 +200,9 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
     // virtual block id in start order: every lower id has started, so the
     // lookback below only waits on blocks that are already running
     pdl_launch_dependents();   // the scatter may launch and stage its first rows
-    if (tid == 0) s_vid = atomicAdd(ticket, 1);   // ticket and flags were cleared before the histogram
     pdl_wait();                                    // the tile histogram is complete and visible
+    // ticket and flags were cleared by the histogram grid
+    if (tid == 0) s_vid = atomicAdd(ticket, 1);
     __syncthreads();
     const int vid = s_vid;
     // warp w owns kScanPerThread consecutive 32-element slices of the block's
@@ -512,6 +519,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
                     }
                 } else {
                     const int lr = a.tok2row[i];
+                    if (e < 0 || e >= E) set_device_error(a.err, MOE_DEVERR_EXPERT_RANGE);
                     if (e >= 0 && e < E && lr >= 0) {
                         const int tile = rt.tile_off[sidx] + (int)((i - item0) / kTileItems);
                         if (kMode == kLowLatency) {
@@ -730,11 +738,10 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
     int32_t *tile_hist = reinterpret_cast<int32_t *>(ws + p.off_hist);
     int32_t *scan = reinterpret_cast<int32_t *>(ws + p.off_scan);
 
-    cudaError_t ce = cudaMemsetAsync(ws, 0, p.off_hist, stream);   // error word, ticket, token counter, lookback flags
-    if (ce != cudaSuccess) return ce;
-
+    cudaError_t ce;
     const size_t hist_smem = (size_t)kHistWarps * E * 4;
-    tile_hist_kernel<<<rt.ntiles, kHistThreads, hist_smem, stream>>>(topk_idx, E, K, rt, tile_hist, tok2row, err);
+    tile_hist_kernel<<<rt.ntiles, kHistThreads, hist_smem, stream>>>(topk_idx, E, K, rt, tile_hist, tok2row, err,
+                                                                     status, p.nscan_blocks);
     if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
 
     const int n = E * rt.ntiles;
@@ -782,10 +789,10 @@ cudaError_t launch_dispatch_ll(const void *x, const int32_t *topk_idx, const Ran
     int32_t *err = reinterpret_cast<int32_t *>(ws);
     int32_t *tile_hist = reinterpret_cast<int32_t *>(ws + p.off_hist);
 
-    cudaError_t ce = cudaMemsetAsync(ws, 0, kWsHeader, stream);   // error word, token counter
-    if (ce != cudaSuccess) return ce;
+    cudaError_t ce;
     const size_t hist_smem = (size_t)kHistWarps * E * 4;
-    tile_hist_kernel<<<rt.ntiles, kHistThreads, hist_smem, stream>>>(topk_idx, E, K, rt, tile_hist, tok2row, err);
+    tile_hist_kernel<<<rt.ntiles, kHistThreads, hist_smem, stream>>>(topk_idx, E, K, rt, tile_hist, tok2row, err,
+                                                                     nullptr, 0);
     if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
 
     ScatterArgs a{};
