@@ -117,7 +117,6 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
     }
 #pragma unroll
     for (int step = 0; step < kItemsPerThread; ++step) {
-        const long long i = lo + warp * kItemsPerWarp + step * 32 + lane;
         int e = e_reg[step];
         if (e >= E) e = -1;   // out of range: no rank (the scatter reports it)
         // lanes holding the same expert: one ballot per bit of the expert id
