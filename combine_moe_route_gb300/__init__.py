@@ -15,7 +15,7 @@ _API = {
     "get_device_error", "abi_version", "strerror", "MoeError", "DispatchResult",
     "moe_layer", "library_path", "load_library", "MOE_OK", "dispatch_noalloc",
     "route_topk_grouped", "dispatch_ll", "combine_ll", "combine_ll_push", "DispatchLLResult",
-    "combine_partial_send", "combine_partial_recv",
+    "combine_partial_send", "combine_partial_recv", "BoundLayer",
 }
 
 __all__ = sorted(_API) + ["workloads", "HostLayerPipeline"]

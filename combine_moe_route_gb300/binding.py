@@ -448,6 +448,76 @@ def moe_layer(x: torch.Tensor, logits: torch.Tensor, B, E: int, K: int, *, fp8: 
     return dict(topk_idx=idx, topk_w=w, dispatch=d, y=y, out=o)
 
 
+class BoundLayer:
+    """One layer's four calls (route, dispatch, expert stand-in, combine) with every tensor
+    checked and every argument marshalled once, for loops that run the same shapes again and
+    again (a decode step run eagerly).  A call then costs one ctypes call per step, with none
+    of the per-call checks.
+
+    The layer reads ``x`` [T, H] bf16 and ``logits`` [T, E] fp32 in place and writes into
+    buffers it owns (``topk_idx``, ``topk_w``, ``dispatch``, ``y``, ``out``).  Refill the
+    inputs in place between calls; do not resize or replace them.  Calls are enqueued on the
+    stream given (default: the current stream at bind time) and on the inputs' device."""
+
+    def __init__(self, x: torch.Tensor, logits: torch.Tensor, B, E: int, K: int, *, fp8: bool = False,
+                 identity: bool = False, out_dtype: torch.dtype = torch.bfloat16, stream=None):
+        dev = x.device
+        self.x, self.logits = x, logits
+        # the regular entry points check every tensor once and allocate the outputs
+        self.topk_idx, self.topk_w = route_topk(logits, K, stream=stream)
+        self.dispatch = dispatch(x, self.topk_idx, B, E, fp8=fp8, stream=stream)
+        d = self.dispatch
+        self.y = expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E, identity=identity, stream=stream)
+        self.out = combine(self.y, d.tok2row, self.topk_w, out_dtype=out_dtype, stream=stream)
+        self._B = _host_B(B)                          # kept alive: the dispatch reads it on each call
+        self._device = dev.index if dev.index is not None else torch.cuda.current_device()
+        T, H = x.shape
+        R = self._B.size
+        st = _stream_handle(stream, dev)
+        lib = load_library()
+        self._calls = (
+            (lib.moe_route_topk, (_ptr(logits), T, E, K, _ptr(self.topk_idx), _ptr(self.topk_w), st),
+             "moe_route_topk"),
+            (lib.moe_dispatch, (_ptr(x), _ptr(self.topk_idx), R, self._B.ctypes.data, E, K, H,
+                                _DTYPE_FP8 if fp8 else _DTYPE_BF16, _ptr(d.recv_x),
+                                _ptr(d.recv_scale) if fp8 else None, _ptr(d.counts), _ptr(d.offsets),
+                                _ptr(d.expert_offsets), _ptr(d.tok2row), _ptr(d.row2src), _ptr(d.workspace),
+                                d.workspace.numel(), st), "moe_dispatch"),
+            (lib.moe_expert_scale, (_ptr(d.recv_x), _ptr(d.recv_scale) if fp8 else None,
+                                    _DTYPE_FP8 if fp8 else _DTYPE_BF16, _ptr(d.expert_offsets), E, H, T * K,
+                                    int(bool(identity)), _ptr(self.y), st), "moe_expert_scale"),
+            (lib.moe_combine, (_ptr(self.y), _ptr(d.tok2row), _ptr(self.topk_w), T, K, H,
+                               _DTYPE_FP32 if out_dtype == torch.float32 else _DTYPE_BF16, _ptr(self.out), st),
+             "moe_combine"),
+        )
+
+    def _run(self, i: int) -> None:
+        fn, args, name = self._calls[i]
+        if torch.cuda.current_device() == self._device:
+            _check(fn(*args), name)
+        else:
+            with torch.cuda.device(self._device):
+                _check(fn(*args), name)
+
+    def route(self) -> None:
+        self._run(0)
+
+    def dispatch_call(self) -> None:
+        self._run(1)
+
+    def expert(self) -> None:
+        self._run(2)
+
+    def combine_call(self) -> None:
+        self._run(3)
+
+    def __call__(self) -> torch.Tensor:
+        """Enqueue the whole layer; returns ``out`` (valid once the stream reaches it)."""
+        for i in range(4):
+            self._run(i)
+        return self.out
+
+
 # ---------------------------------------------------------------------------
 # dispatch without a caller-supplied workspace
 # ---------------------------------------------------------------------------
