@@ -273,6 +273,25 @@ def measure_decode_layouts(dev, stream, flush):
     res["graph_ragged_dispatch_plus_combine_us"] = time_flushed(g.replay, stream, flush)
     res["graph_ll_dispatch_plus_combine_us"] = time_flushed(gl.replay, stream, flush)
     res["graph_ll_unordered_dispatch_plus_combine_us"] = time_flushed(gu.replay, stream, flush)
+    # whole eager decode layers (route, dispatch, expert stand-in, combine) enqueued back to back:
+    # through the package functions, whose per-call checks cost host time, and through BoundLayer
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    bound = b.BoundLayer(x, logits, B, E, K)
+
+    def eager_us(fn, n=50):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        z.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(z) * 1e3 / n
+
+    res["eager_layer_package_us"] = eager_us(lambda: b.moe_layer(x, logits, B, E, K))
+    res["eager_layer_bound_us"] = eager_us(bound)
     db = dispatch_bytes(T, E, R, K, H, False)
     cb = combine_bytes(T, K, H)
     res["floor_us_at_8TBs"] = {"dispatch": db / 8e6, "combine": cb / 8e6}
