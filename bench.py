@@ -18,6 +18,7 @@ layer; ranks do not exchange data.  ``--impl reference`` times the CPU oracle
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -205,18 +206,28 @@ def time_call(fn, stream, reps: int = 50) -> float:
 
 
 def time_flushed(fn, stream, flush, reps: int = 50) -> float:
-    """Mean µs of fn() with the L2 flushed (outside the events) before every call."""
+    """Median µs of fn() with the L2 flushed (outside the events) before every call.
+
+    A call here is tens of µs of GPU work, so a host pause of a millisecond (a garbage
+    collection) can drain the queue inside one sample; the collector is off while the calls
+    are enqueued, and the median ignores a stray sample."""
     for _ in range(3):
         fn()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
     torch.cuda.synchronize()
-    for a, z in ev:
-        flush.fill_(3)
-        a.record(stream)
-        fn()
-        z.record(stream)
-    torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(z) for a, z in ev) * 1e3
+    gc_was_on = gc.isenabled()
+    gc.disable()
+    try:
+        for a, z in ev:
+            flush.fill_(3)
+            a.record(stream)
+            fn()
+            z.record(stream)
+        torch.cuda.synchronize()
+    finally:
+        if gc_was_on:
+            gc.enable()
+    return statistics.median(a.elapsed_time(z) for a, z in ev) * 1e3
 
 
 def measure_decode_layouts(dev, stream, flush):
