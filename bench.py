@@ -252,6 +252,8 @@ def measure_decode_layouts(dev, stream, flush):
     outl = b.combine_ll(yl, E, R, C, dl.tok2row, wts)
     ret = b.combine_ll_push(yl, dl, R, E, T, K)
     du = b.dispatch_ll(x, idx, B, E, C, unordered=True)      # slots by atomic increments, no histogram
+    dl8 = b.dispatch_ll(x, idx, B, E, C, fp8=True)           # the FP8 payload the sources send by default
+    du8 = b.dispatch_ll(x, idx, B, E, C, fp8=True, unordered=True)
     yu = b.expert_scale(du.recv_x, None, eo, E)
     outu = b.combine_ll(yu, E, R, C, du.tok2row, wts)
     torch.cuda.synchronize()
@@ -261,6 +263,9 @@ def measure_decode_layouts(dev, stream, flush):
         "ll_dispatch_us": time_flushed(lambda: b.dispatch_ll(x, idx, B, E, C, out=dl), stream, flush),
         "ll_unordered_dispatch_us": time_flushed(
             lambda: b.dispatch_ll(x, idx, B, E, C, unordered=True, out=du), stream, flush),
+        "ll_fp8_dispatch_us": time_flushed(lambda: b.dispatch_ll(x, idx, B, E, C, fp8=True, out=dl8), stream, flush),
+        "ll_unordered_fp8_dispatch_us": time_flushed(
+            lambda: b.dispatch_ll(x, idx, B, E, C, fp8=True, unordered=True, out=du8), stream, flush),
         "ll_combine_gather_us": time_flushed(lambda: b.combine_ll(yl, E, R, C, dl.tok2row, wts, out=outl),
                                              stream, flush),
         "ll_combine_push_us": time_flushed(lambda: b.combine_ll_push(yl, dl, R, E, T, K, out=ret), stream, flush),
