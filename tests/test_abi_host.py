@@ -171,6 +171,83 @@ def test_route_grouped_validation(lib):
     assert f(None, 0, 256, 8, 8, 4, None, None, None) == OK
 
 
+def _dispatch_ll(lib, unordered, B, E=16, K=2, H=256, C=8, dtype=BF16, x=FAKE, recv=FAKE, scale=FAKE, counts=FAKE,
+                 ws=FAKE, ws_bytes=1 << 30):
+    f = lib.moe_dispatch_ll_unordered if unordered else lib.moe_dispatch_ll
+    return f(x, FAKE, B.size, B.ctypes.data, E, K, H, C, dtype, recv, scale, counts, FAKE, FAKE, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("unordered", [False, True])
+def test_dispatch_ll_validation(lib, unordered):
+    # T = 0 is left out on purpose: it zeroes counts, which here is a fake pointer
+    B = _B(3, 0, 5, 1)
+    assert _dispatch_ll(lib, unordered, _B()) == INVALID                                # R = 0
+    assert _dispatch_ll(lib, unordered, B, E=18) == INVALID                             # E % R
+    assert _dispatch_ll(lib, unordered, B, K=17) == INVALID                             # K > E
+    assert _dispatch_ll(lib, unordered, B, H=12) == INVALID                             # H % 8
+    assert _dispatch_ll(lib, unordered, B, H=264, dtype=FP8) == INVALID                 # FP8 needs H % 128
+    assert _dispatch_ll(lib, unordered, B, dtype=FP32) == INVALID                       # no fp32 payload
+    assert _dispatch_ll(lib, unordered, B, C=0) == INVALID                              # no slots
+    assert _dispatch_ll(lib, unordered, B, E=1024, C=1 << 19) == INVALID                # E*R*C overflows int32
+    assert _dispatch_ll(lib, unordered, B, C=4) == INVALID                              # B[2] = 5 > C
+    assert _dispatch_ll(lib, unordered, _B(3, -1, 5, 1)) == INVALID                     # negative B
+    assert _dispatch_ll(lib, unordered, B, counts=None) == INVALID
+    assert _dispatch_ll(lib, unordered, B, x=None) == INVALID
+    assert _dispatch_ll(lib, unordered, B, dtype=FP8, scale=None) == INVALID
+    assert _dispatch_ll(lib, unordered, B, ws=None) == WORKSPACE
+    assert _dispatch_ll(lib, unordered, B, ws_bytes=255) == WORKSPACE                   # less than the header
+    # the ordered form needs the histogram workspace; the unordered one the 256-byte header only
+    header_only = _dispatch_ll(lib, unordered, B, x=FAKE_MISALIGNED, ws_bytes=256)
+    assert header_only == (UNSUPPORTED if unordered else WORKSPACE)
+    assert _dispatch_ll(lib, unordered, B, recv=FAKE_MISALIGNED) == UNSUPPORTED
+    assert _dispatch_ll(lib, unordered, B, ws=FAKE_MISALIGNED) == UNSUPPORTED
+    assert _dispatch_ll(lib, unordered, B, dtype=FP8, scale=FAKE_MISALIGNED) == UNSUPPORTED
+
+
+def test_combine_ll_validation(lib):
+    c = lib.moe_combine_ll                  # (y, E, R, C, tok2row, w, T, K, H, out_dtype, out, stream)
+    assert c(FAKE, 16, 4, 8, FAKE, FAKE, -1, 2, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE, 16, 4, 8, FAKE, FAKE, 4, 0, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE, 16, 4, 8, FAKE, FAKE, 4, 33, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE, 0, 4, 8, FAKE, FAKE, 4, 2, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE, 16, 0, 8, FAKE, FAKE, 4, 2, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE, 16, 4, 0, FAKE, FAKE, 4, 2, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE, 1024, 256, 1 << 13, FAKE, FAKE, 4, 2, 256, BF16, FAKE, None) == INVALID   # E*R*C = 2^31
+    assert c(FAKE, 16, 4, 8, FAKE, FAKE, 4, 2, 250, BF16, FAKE, None) == INVALID
+    assert c(FAKE, 16, 4, 8, FAKE, FAKE, 4, 2, 256, FP8, FAKE, None) == INVALID
+    assert c(FAKE, 16, 4, 8, None, FAKE, 4, 2, 256, BF16, FAKE, None) == INVALID     # no identity map here
+    assert c(None, 16, 4, 8, FAKE, FAKE, 4, 2, 256, BF16, FAKE, None) == INVALID
+    assert c(FAKE_MISALIGNED, 16, 4, 8, FAKE, FAKE, 4, 2, 256, BF16, FAKE, None) == UNSUPPORTED
+    assert c(FAKE, 16, 4, 8, FAKE, FAKE, 4, 2, 256, FP32, FAKE_MISALIGNED, None) == UNSUPPORTED
+    assert c(None, 16, 4, 8, None, None, 0, 2, 256, BF16, None, None) == OK
+    p = lib.moe_combine_ll_push             # (y, row2src, counts, R, E, C, K, H, T, ret, stream)
+    assert p(FAKE, FAKE, FAKE, 0, 16, 8, 2, 256, 4, FAKE, None) == INVALID
+    assert p(FAKE, FAKE, FAKE, 4, 16, 8, 33, 256, 4, FAKE, None) == INVALID
+    assert p(FAKE, FAKE, FAKE, 4, 16, 8, 2, 12, 4, FAKE, None) == INVALID
+    assert p(FAKE, None, FAKE, 4, 16, 8, 2, 256, 4, FAKE, None) == INVALID
+    assert p(FAKE, FAKE, None, 4, 16, 8, 2, 256, 4, FAKE, None) == INVALID
+    assert p(FAKE, FAKE, FAKE, 4, 16, 8, 2, 256, 4, FAKE_MISALIGNED, None) == UNSUPPORTED
+    assert p(None, None, None, 4, 16, 8, 2, 256, 0, None, None) == OK
+
+
+def test_combine_partial_validation(lib):
+    s = lib.moe_combine_partial_send        # (y, tok2row, idx, w, T, K, H, E, R, partial, stream)
+    assert s(FAKE, FAKE, FAKE, FAKE, 4, 2, 256, 18, 4, FAKE, None) == INVALID        # E % R
+    assert s(FAKE, FAKE, FAKE, FAKE, 4, 2, 256, 512, 512, FAKE, None) == INVALID     # R > 256
+    assert s(FAKE, FAKE, FAKE, FAKE, 4, 17, 256, 16, 4, FAKE, None) == INVALID       # K > E
+    assert s(FAKE, FAKE, FAKE, FAKE, 4, 2, 12, 16, 4, FAKE, None) == INVALID         # H % 8
+    assert s(FAKE, FAKE, None, FAKE, 4, 2, 256, 16, 4, FAKE, None) == INVALID
+    assert s(FAKE, FAKE, FAKE, FAKE, 4, 2, 256, 16, 4, FAKE_MISALIGNED, None) == UNSUPPORTED
+    assert s(None, None, None, None, 0, 2, 256, 16, 4, None, None) == OK
+    r = lib.moe_combine_partial_recv        # (partial, idx, T, K, H, E, R, out_dtype, out, stream)
+    assert r(FAKE, FAKE, -1, 2, 256, 16, 4, BF16, FAKE, None) == INVALID
+    assert r(FAKE, FAKE, 4, 2, 256, 18, 4, BF16, FAKE, None) == INVALID
+    assert r(FAKE, FAKE, 4, 2, 256, 16, 4, FP8, FAKE, None) == INVALID
+    assert r(FAKE, None, 4, 2, 256, 16, 4, BF16, FAKE, None) == INVALID
+    assert r(FAKE_MISALIGNED, FAKE, 4, 2, 256, 16, 4, BF16, FAKE, None) == UNSUPPORTED
+    assert r(None, None, 0, 2, 256, 16, 4, FP32, None, None) == OK
+
+
 def test_plain_c_consumer_compiles_and_links(lib, tmp_path):
     """The C ABI needs nothing but its header and the CUDA runtime: a plain C11 program
     (tests/c_abi/roundtrip.c) compiles without warnings and links against the library."""
