@@ -7,9 +7,10 @@
 //
 // One warp per token.  Lane l holds logits e = l, l+32, l+64, ... in
 // registers as an order-preserving 32-bit image of each fp32 value.  The
-// K-th largest lane maximum tau (K rounds of redux.sync over the lane maxima)
-// is a lower bound of the row's K-th largest key, so the top K is among the
-// candidates key >= tau -- on random rows K plus a few.  The candidates are
+// K-th largest lane maximum, its lowest 5 bits replaced by a lane tag so that
+// K rounds of one redux.sync each find it, gives tau, a lower bound of the
+// row's K-th largest key, so the top K is among the candidates key >= tau --
+// on random rows K plus a few.  The candidates are
 // compacted into shared memory and each one's output position is the number
 // of candidates ahead of it (larger key, or equal key and smaller id).  Rows
 // with more than kMaxCandidates candidates (many equal keys) instead take K
@@ -124,26 +125,31 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
             if (slot_group[i] >= 32 || !((kept >> slot_group[i]) & 1u)) avail &= ~(1u << i);
     }
 
-    // Threshold: tau = the K-th largest of the 32 lane maxima.  The K lanes
-    // with the largest maxima hold K keys >= tau, so the K-th largest key of
-    // the row is >= tau, and every member of the top K (ties included) is a
-    // candidate: an eligible key >= tau.  On random rows only a few keys
-    // beyond K pass.
+    // Threshold.  Each lane's maximum keeps its upper 27 bits and takes the
+    // tag 31 - lane in its lower 5, so the 32 tagged values are distinct and
+    // each of K rounds retires exactly one of them with a single redux.sync.
+    // tau = the upper 27 bits of the K-th largest tagged value.  The K retired
+    // lanes each hold a key >= tau, so the K-th largest key of the row is
+    // >= tau, and every member of the top K (ties included) is a candidate:
+    // an eligible key >= tau.  Truncating only lowers tau, which admits a few
+    // more candidates, never fewer.  If fewer than K lanes hold a key, the
+    // rounds run out (top = 0) and every eligible key is a candidate.  On
+    // random rows only a few keys beyond K pass.
     uint32_t ek[NPL];   // eligible keys; 0 = not eligible (every real key is > 0)
     uint32_t lmax = 0u;
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
-        ek[i] = (avail & (1u << i)) ? key[i] : 0u;
+        // the plain top-K keeps every in-range slot; key[i] is already 0 past E
+        ek[i] = (G <= 1 || (avail & (1u << i))) ? key[i] : 0u;
         lmax = max(lmax, ek[i]);
     }
-    uint32_t tau = 0u;
+    uint32_t v = lmax ? ((lmax & ~31u) | (uint32_t)(31 - lane)) : 0u;
+    uint32_t top = 0u;
     for (int k = 0; k < K; ++k) {
-        const uint32_t top = __reduce_max_sync(0xffffffffu, lmax);
-        tau = top;
-        if (top == 0u) break;   // fewer than K lanes hold a key: every eligible key is a candidate
-        const uint32_t who = __reduce_min_sync(0xffffffffu, (lmax == top) ? (uint32_t)lane : 32u);
-        if ((uint32_t)lane == who) lmax = 0u;
+        top = __reduce_max_sync(0xffffffffu, v);
+        if (v == top) v = 0u;   // the one lane holding top (top = 0: nothing left, no change)
     }
+    const uint32_t tau = top & ~31u;
     uint32_t cm = 0u;   // bit i: slot i is a candidate
 #pragma unroll
     for (int i = 0; i < NPL; ++i)
