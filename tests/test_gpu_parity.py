@@ -241,6 +241,7 @@ SHAPES = [
     (2, 2, 2, 16, [3, 0]),                     # K == E == R, an empty rank
     (3, 9, 3, 256, [0, 700, 5]),               # K = 3: tokens straddle 2048-item tiles
     (3, 12, 2, 384, [1025, 1024, 1023]),       # odd number of 128-blocks (FP8)
+    (2, 8, 2, 1280, [33, 20]),                 # 10 blocks: a full step of the in-place quantiser and a part
     (8, 16, 2, 256, [64, 1, 0, 33, 64, 2, 17, 5]),
     (8, 64, 8, 7168, [300, 0, 1, 257, 0, 0, 512, 3]),
     (4, 1024, 32, 128, [40, 0, 3, 9]),         # E and K at their limits

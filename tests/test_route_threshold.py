@@ -1,0 +1,62 @@
+"""The bound behind the route kernel's candidate filter (CPU only).
+
+The kernel keeps one warp per token; lane l holds the keys of experts l, l+32, ... .
+Its threshold tau is the upper 27 bits of the K-th largest of the 32 lane maxima, each
+with its low 5 bits replaced by the tag 31 - l (a lane without keys contributes 0), and
+every eligible key >= tau becomes a candidate.  The selection is exact only if the
+candidates hold the whole top K (key descending, equal keys by smaller expert), which is
+what these rows check: random, tie-heavy and denormal rows, and shapes where fewer than
+K lanes hold keys.  The keys are the order-preserving image of fp32 (after adding +0)."""
+import numpy as np
+import pytest
+
+
+def _keys(f):
+    u = (f.astype(np.float32) + np.float32(0.0)).view(np.uint32).astype(np.uint64)
+    return np.where((u >> 31) == 1, (~u) & 0xFFFFFFFF, u | 0x80000000)
+
+
+def _tagged_tau(k, K):
+    E = k.size
+    lanes = np.zeros((32, -(-E // 32)), np.uint64)
+    for e in range(E):
+        lanes[e % 32, e // 32] = k[e]
+    lmax = lanes.max(axis=1)
+    v = np.where(lmax > 0, (lmax & ~np.uint64(31)) | (31 - np.arange(32)).astype(np.uint64), 0)
+    top = 0
+    for _ in range(K):
+        top = int(v.max())
+        v[v == top] = 0          # the tags make the one lane holding top unique (top = 0: no change)
+    return top & ~31
+
+
+@pytest.mark.parametrize("E,K", [(256, 8), (32, 32), (40, 33), (9, 3), (1024, 32), (384, 8), (64, 1)])
+@pytest.mark.parametrize("kind", ["normal", "ties", "denormal"])
+def test_candidates_hold_the_top_k(E, K, kind):
+    rng = np.random.default_rng(E * 100 + K)
+    for _ in range(150):
+        if kind == "normal":
+            f = rng.standard_normal(E)
+        elif kind == "ties":
+            f = np.round(rng.standard_normal(E) * 2.0)
+        else:
+            f = rng.integers(-3, 4, E) * np.float32(1e-45)
+        k = _keys(np.asarray(f, np.float32))
+        order = np.lexsort((np.arange(E), -k.astype(np.int64)))
+        tau = _tagged_tau(k, K)
+        cand = np.flatnonzero((k != 0) & (k >= tau))
+        assert set(order[:K].tolist()) <= set(cand.tolist())
+
+
+def test_fewer_lanes_than_k_admits_every_key():
+    # E = 40, K = 33: 32 lanes hold keys, so the 33rd round finds nothing and tau = 0
+    k = _keys(np.random.default_rng(3).standard_normal(40).astype(np.float32))
+    assert _tagged_tau(k, 33) == 0
+
+
+def test_random_rows_admit_few_candidates():
+    # DeepSeek-V3 router shape: about K plus one candidates per row on N(0, 1) logits
+    rng = np.random.default_rng(11)
+    n = [int(((k := _keys(rng.standard_normal(256).astype(np.float32))) >= _tagged_tau(k, 8)).sum())
+         for _ in range(400)]
+    assert 8 <= min(n) and np.mean(n) < 10 and max(n) <= 64
