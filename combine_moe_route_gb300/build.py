@@ -8,6 +8,7 @@ combine_moe_route_gb300.build`` runs it from the command line.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -63,8 +64,20 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
     build is always redone."""
     if out_dir is None and not defines and not force and up_to_date():
         return library_path()
+    default = out_dir is None and not defines
     out_dir = out_dir or OUT_DIR
     os.makedirs(out_dir, exist_ok=True)
+    # one build of a folder at a time: parallel processes (test workers) would
+    # otherwise write the same object files; a caller that waited finds the
+    # library already up to date
+    with open(os.path.join(out_dir, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if default and not force and up_to_date():
+            return library_path()
+        return _compile_and_link(out_dir, ptxas_info, verbose, defines)
+
+
+def _compile_and_link(out_dir: str, ptxas_info: bool, verbose: bool, defines: tuple[str, ...]) -> str:
     exe = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
     extra += [f"-D{d}" for d in defines]
