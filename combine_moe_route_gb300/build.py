@@ -71,7 +71,10 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
     # otherwise write the same object files; a caller that waited finds the
     # library already up to date
     with open(os.path.join(out_dir, ".lock"), "w") as lock:
-        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            fcntl.flock(lock, fcntl.LOCK_EX)
+        except OSError:   # a file system without locks: build unlocked, as a single process would
+            pass
         if default and not force and up_to_date():
             return library_path()
         return _compile_and_link(out_dir, ptxas_info, verbose, defines)
