@@ -3,11 +3,10 @@
 //
 // Who needs it: code that runs where allocation is not allowed or not
 // possible -- for example a plugin inside another inference engine whose
-// memory is owned and budgeted by that engine, a serving loop that must not
+// memory is owned and budgeted by that engine, or a serving loop that must not
 // allocate on its hot path (an allocation can block, fragment a caching
-// allocator or fail under memory pressure), or a caller recording a CUDA
-// graph, during which a plain cudaMalloc is not permitted.  Such a caller can
-// still pass its inputs and outputs, but not moe_dispatch's workspace.
+// allocator or fail under memory pressure).  Such a caller can still pass its
+// inputs and outputs, but not moe_dispatch's workspace.
 //
 // This variant takes its workspace from a fixed array in device memory that
 // the library owns: a file-scope static __device__ buffer of

@@ -201,8 +201,9 @@ MOE_API moe_status moe_dispatch(const void *x, const int32_t *topk_idx,
 /*
  * moe_dispatch_noalloc -- moe_dispatch without a caller-supplied workspace,
  * for callers that cannot allocate device memory: a plugin whose memory is
- * owned by a host framework, a serving loop that must not allocate on its hot
- * path, or code recording a CUDA graph (where cudaMalloc is not permitted).
+ * owned and budgeted by a host framework, or a serving loop that must not
+ * allocate on its hot path (an allocation can block, or fail under memory
+ * pressure).
  * The pages this library follows have no counterpart to it.
  *
  * Arguments and outputs are those of moe_dispatch, minus the workspace.  The

@@ -1,7 +1,7 @@
 """moe_dispatch_noalloc: the dispatch entry point for callers that cannot
-allocate device memory (a plugin whose memory belongs to a host framework, a
-serving loop that must not allocate on its hot path, code recording a CUDA
-graph).  It uses the library's static device scratch instead of a workspace.
+allocate device memory (a plugin whose memory belongs to a host framework, or
+a serving loop that must not allocate on its hot path).  It uses the library's
+static device scratch instead of a workspace.
 
 Called here through the C ABI with ctypes; every output must equal, bit for
 bit, what moe_dispatch (with a caller workspace) produces for the same input
