@@ -24,9 +24,11 @@
  *     device; pointers marked "host" are ordinary host memory read during the
  *     call.  The caller allocates and owns every buffer; the library never
  *     allocates, frees or synchronises (except moe_get_device_error, which
- *     says so).  Work is enqueued on `stream` and runs asynchronously; the
- *     calls take no host-device synchronisation, so a sequence of them can be
- *     captured in a CUDA graph ([DSD] "CUDA Graph").
+ *     says so).  Work is enqueued on `stream` and runs asynchronously, and
+ *     the calls take no host-device synchronisation.  A layer of
+ *     moe_route_topk, moe_dispatch (or moe_dispatch_ll[_unordered]),
+ *     moe_expert_scale and moe_combine (or moe_combine_ll) can therefore be
+ *     captured in a CUDA graph and replayed ([DSD] "CUDA Graph").
  *   - Arrays are dense, row-major, with no padding between rows.
  *   - Arguments are validated on the host before anything is enqueued; a bad
  *     argument returns MOE_ERR_INVALID_ARG (or MOE_ERR_UNSUPPORTED for a
