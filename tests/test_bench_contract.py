@@ -1,0 +1,102 @@
+"""bench.py's output contract, on the CPU.
+
+The GPU arm needs a GPU; what can be checked here is the reference arm (the
+CPU oracle timed on a sample of the workload), its behaviour under two ranks,
+and the algorithmic-byte accounting that the roofline fraction divides by."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CONTRACT_KEYS = {"impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                 "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"}
+
+
+def _json_lines(text):
+    out = []
+    for line in text.splitlines():
+        line = line.strip()
+        if line.startswith("{"):
+            out.append(json.loads(line))
+    return out
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "toy", "--steps", "2",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    d = lines[0]
+    assert CONTRACT_KEYS <= set(d)
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["higher_is_better"] is False and d["vs_baseline"] is None and d["data"] == "synthetic"
+    assert d["unit"] == "us/layer" and d["value"] > 0
+    assert d["config"]["workload"] == "toy"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_warmup_is_at_least_three():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "toy", "--steps", "1",
+                        "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    (d,) = _json_lines(r.stdout)
+    assert d["warmup"] == 3
+
+
+def test_reference_arm_under_two_ranks_prints_once():
+    # torchrun with two gloo ranks on this host: rank 0 alone times the oracle
+    # and prints; rank 1 exits 0 without work.  On a machine with a GPU the
+    # ranks would take NCCL and one GPU each, so it needs two there.
+    import torch
+    if torch.cuda.is_available() and torch.cuda.device_count() < 2:
+        pytest.skip("two ranks on a CUDA machine need two GPUs")
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
+           "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference", "--workload", "toy",
+           "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+@pytest.mark.parametrize("name", ["dsv3_decode", "dsv3_prefill"])
+def test_algorithmic_bytes_of_the_deepseek_layers(name):
+    # The per-layer bytes each call must move, term by term: the source rows
+    # read once, K copies written once (1 byte per channel in FP8, 2 in bf16),
+    # the fp32 scale per 128 channels, the routing read, both maps written and
+    # the count matrices; the combine reads K bf16 rows per token, writes one,
+    # and reads the weights and the gather map.
+    sys.path.insert(0, ROOT)
+    import bench
+    from combine_moe_route_gb300 import workloads as wl
+    w = wl.WORKLOADS[name]
+    T = int(wl.draw_B(w, 0).sum())
+    assert T == (32768 if name == "dsv3_prefill" else 1024)
+    rows = T * w.K
+    src = T * w.H * 2
+    copies = rows * w.H * (1 if w.fp8 else 2)
+    scales = rows * (w.H // 128) * 4 if w.fp8 else 0
+    maps = rows * 4 + 2 * rows * 4 + 2 * w.E * w.R * 4
+    assert bench.dispatch_bytes(T, w.E, w.R, w.K, w.H, w.fp8) == src + copies + scales + maps
+    assert bench.combine_bytes(T, w.K, w.H) == rows * w.H * 2 + T * w.H * 2 + 2 * rows * 4
+    # the figures quoted beside the measurements, in MB
+    want = {"dsv3_prefill": (2410.7, 4230.0), "dsv3_decode": (132.2, 132.2)}[name]
+    assert round(bench.dispatch_bytes(T, w.E, w.R, w.K, w.H, w.fp8) / 1e6, 1) == want[0]
+    assert round(bench.combine_bytes(T, w.K, w.H) / 1e6, 1) == want[1]
