@@ -61,6 +61,22 @@ def route_bytes(T, E, K):
     return T * E * 4 + T * K * 8
 
 
+def routing_load(counts, E: int, R: int) -> dict:
+    """How evenly the routing spreads the rows, from dispatch's count matrix
+    (counts[e*R + s] = tokens of rank s routed to expert e): rows per expert
+    and rows per destination rank (its E/R experts), max, min and max/mean."""
+    c = np.asarray(counts, dtype=np.int64).reshape(E, R)
+    per_expert = c.sum(axis=1)
+    per_rank = per_expert.reshape(R, E // R).sum(axis=1)
+
+    def stats(v):
+        mean = float(v.mean())
+        return {"max": int(v.max()), "min": int(v.min()), "mean": mean,
+                "max_over_mean": float(v.max()) / mean if mean > 0 else None}
+
+    return {"rows_per_expert": stats(per_expert), "rows_per_dest_rank": stats(per_rank)}
+
+
 # ---------------------------------------------------------------------------
 # environment helpers
 # ---------------------------------------------------------------------------
@@ -713,6 +729,7 @@ def run_ours(args, world, rank, local):
     else:
         line_note = None
     clk = clocks.summary()
+    load = routing_load(d.counts.cpu().numpy(), E, w.R)
     line = {
         "metric": METRIC,
         "value": replica_value(dc_us_max, world),
@@ -737,6 +754,7 @@ def run_ours(args, world, rank, local):
                 "combine_GBps": c_gbs, "combine_pct_of_8TBs": 100 * c_gbs / NOMINAL_HBM_GBS,
                 "dispatch_frac_of_measured": d_gbs / peak, "combine_frac_of_measured": c_gbs / peak,
                 "route_GBps": route_bytes(T, E, K) / (r_us * 1e-6) / 1e9},
+        "routing_load": load,
         "p50_us": {"dispatch": statistics.median(disp_ms) * 1e3, "combine": statistics.median(comb_ms) * 1e3},
         "p10_p90_us": {"dispatch": pct(disp_ms), "combine": pct(comb_ms)},
         "unflushed_us": unflushed,

@@ -9,6 +9,7 @@ import socket
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -100,3 +101,36 @@ def test_algorithmic_bytes_of_the_deepseek_layers(name):
     want = {"dsv3_prefill": (2410.7, 4230.0), "dsv3_decode": (132.2, 132.2)}[name]
     assert round(bench.dispatch_bytes(T, w.E, w.R, w.K, w.H, w.fp8) / 1e6, 1) == want[0]
     assert round(bench.combine_bytes(T, w.K, w.H) / 1e6, 1) == want[1]
+
+
+def test_routing_load_summary():
+    sys.path.insert(0, ROOT)
+    import bench
+    # E = 4 experts on R = 2 ranks; counts[e*R + s]
+    counts = np.array([3, 1,    # expert 0: 4 rows
+                       0, 0,    # expert 1: 0
+                       2, 2,    # expert 2: 4
+                       4, 0])   # expert 3: 4
+    got = bench.routing_load(counts, 4, 2)
+    assert got["rows_per_expert"] == {"max": 4, "min": 0, "mean": 3.0, "max_over_mean": 4 / 3}
+    # destination rank 0 holds experts 0-1 (4 rows), rank 1 experts 2-3 (8 rows)
+    assert got["rows_per_dest_rank"] == {"max": 8, "min": 4, "mean": 6.0, "max_over_mean": 8 / 6}
+    assert bench.routing_load(np.zeros(8, np.int32), 4, 2)["rows_per_expert"]["max_over_mean"] is None
+
+
+def test_routing_load_shows_the_zipf_skew(oracle):
+    # the Kimi-K2-style workload adds a Zipf(1.2) bias per expert to the logits,
+    # so its rows pile onto a few experts; the toy workload's N(0,1) logits do not
+    sys.path.insert(0, ROOT)
+    import bench
+    from combine_moe_route_gb300 import workloads as wl
+    ratios = {}
+    for name in ("toy", "kimi_decode"):
+        w = wl.WORKLOADS[name]
+        inp = wl.generate(w, 0)
+        idx, _ = oracle.route_topk(inp["logits"], w.K)
+        d = oracle.dispatch(np.zeros((inp["T"], 8), np.uint16), idx, inp["B"], w.E)   # counts need no payload
+        load = bench.routing_load(d["counts"], w.E, w.R)
+        assert load["rows_per_expert"]["mean"] * w.E == inp["T"] * w.K
+        ratios[name] = load["rows_per_expert"]["max_over_mean"]
+    assert ratios["toy"] < 2.0 < 10.0 < ratios["kimi_decode"]
