@@ -210,18 +210,35 @@ def test_page_counting_examples(oracle):
         B = np.full(R, T // R, np.int32)
         B[: T - int(B.sum())] += 1
         rng = np.random.default_rng(9)
+        L = E // R
         if name in ("max_active_experts", "mean_active_experts_per_rank"):
             # two tokens routed to disjoint expert sets reach the printed maximum
             perm = rng.permutation(E)
             idx = perm[: T * K].reshape(T, K).astype(np.int32)
+        elif name.startswith("worst_case_rows_per_rank"):
+            # every token sends as many copies as it can to rank 0: all of its
+            # experts there when K <= E/R, else all E/R of rank 0's and the rest
+            # on the next rank
+            loc = min(K, L)
+            one = np.array(list(range(loc)) + list(range(L, L + K - loc)), np.int32)
+            idx = np.tile(one, (T, 1))
         else:
             logits = wl.draw_logits(T, E, rng)
             idx, _ = oracle.route_topk(logits, K)
         d = oracle.dispatch(np.zeros((T, 8), np.uint16), idx, B, E)
         per_expert = d["counts"].reshape(E, R).sum(1)
         active = per_expert > 0
-        L = E // R
-        if name == "max_active_experts":
+        if name.startswith("worst_case_rows_per_rank"):
+            eo = d["expert_offsets"]
+            got = int(eo[L] - eo[0])                      # rank 0's receive window
+            assert got <= T * max(K, L)                   # the page's printed bound holds
+            # and no routing gives any rank more: random routings of the same shape
+            for seed in range(20):
+                r_idx = np.stack([np.random.default_rng(seed * 1000 + g).permutation(E)[:K]
+                                  for g in range(T)]).astype(np.int32)
+                r_eo = oracle.dispatch(np.zeros((T, 8), np.uint16), r_idx, B, E)["expert_offsets"]
+                assert np.all(r_eo[L::L] - r_eo[:-1:L] <= expect)
+        elif name == "max_active_experts":
             got = int(active.sum())
             assert got <= T * K
         elif name in ("mean_active_experts_per_rank",):
@@ -236,7 +253,8 @@ def test_page_counting_examples(oracle):
             raise AssertionError(name)
         assert got == expect, (name, got, expect)
     assert seen == {"max_active_experts", "mean_active_experts_per_rank",
-                    "active_experts_per_rank_large_batch", "mean_tokens_per_expert"}
+                    "active_experts_per_rank_large_batch", "mean_tokens_per_expert",
+                    "worst_case_rows_per_rank", "worst_case_rows_per_rank_few_local_experts"}
 
 
 # --------------------------------------------------------------------------
