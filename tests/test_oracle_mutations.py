@@ -133,6 +133,42 @@ MUTATIONS = [
      "acc = acc + oracle_f32_from_bf16(wire);",
      "acc = acc + part;",
      [P.test_partial_with_one_rank_is_receive_side, P.test_partial_slots_and_error_bound]),
+    ("route never marks a chosen expert (the same one picked K times)",
+     "chosen[best] = 1;\n            topk_idx[(size_t)g * K + j] = best;\n        }\n        double m",
+     "chosen[best] = 0;\n            topk_idx[(size_t)g * K + j] = best;\n        }\n        double m",
+     [P.test_route_k_equals_e_is_stable_descending_sort, P.test_route_brute_force_tiny]),
+    ("expert offsets read at e instead of e*R",
+     "for (int e = 0; e <= E; ++e) expert_offsets[e] = offsets[e * R];",
+     "for (int e = 0; e <= E; ++e) expert_offsets[e] = offsets[e];",
+     [P.test_dispatch_matches_library_stable_sort]),
+    ("inverse quantisation scale as 1/scale instead of 448/amax",
+     "float inv = 448.0f / amax;",
+     "float inv = 1.0f / s;",
+     [F.test_block_quant_matches_library_ops, F.test_block_quant_error_bound_and_amax_code]),
+    ("every block of a row keeps the first block's scale",
+     "scale[b] = s;",
+     "scale[0] = s;",
+     [F.test_block_quant_matches_library_ops]),
+    ("e4m3 rounding ties up instead of to even",
+     "if (frac > 0.5f || (frac == 0.5f && (i & 1u))) i += 1u;",
+     "if (frac >= 0.5f) i += 1u;",
+     [F.test_e4m3_encode_matches_library_inside_range, F.test_e4m3_encode_rounding_and_saturation]),
+    ("FP8 expert stand-in dequantises with the row's first block scale",
+     "xhat = oracle_e4m3_decode(q) * recv_scale[(int64_t)row * (H / 128) + h / 128];",
+     "xhat = oracle_e4m3_decode(q) * recv_scale[(int64_t)row * (H / 128)];",
+     [P.test_expert_scale_matches_library_ops]),
+    ("combine gathers the first copy's row for every j",
+     "int32_t row = tok2row[g * K + j];\n                float v",
+     "int32_t row = tok2row[g * K];\n                float v",
+     [P.test_combine_one_hot_weights_pick_the_row, P.test_combine_identity_experts_returns_input]),
+    ("combine rounds the running sum to bf16 after every term",
+     "acc = fmaf(topk_w[g * K + j], v, acc);",
+     "acc = oracle_f32_from_bf16(oracle_bf16_from_f32(fmaf(topk_w[g * K + j], v, acc)));",
+     [P.test_combine_fp32_within_error_bound_of_exact]),
+    ("partial stored in the slot of the last copy on that rank",
+     "if (j0 < 0) j0 = j;",
+     "j0 = j;",
+     [P.test_partial_slots_and_error_bound]),
 ]
 
 
