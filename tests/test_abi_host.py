@@ -112,6 +112,37 @@ def test_dispatch_validation(lib):
     assert _dispatch(lib, B, dtype=FP8, scale=FAKE_MISALIGNED) == UNSUPPORTED
 
 
+def test_dispatch_noalloc_size_validation(lib):
+    # Only the rejections that come before the first CUDA call on every machine:
+    # sizes that moe_dispatch rejects (passed through with its status) and
+    # sizes whose workspace exceeds the static scratch.  Shapes that pass those
+    # first look up the scratch's device address, so they are not called here.
+    import ctypes
+    f = lib.moe_dispatch_noalloc
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    f.restype = i32
+
+    def call(B, E=16, K=2, H=256, dtype=BF16, R=None):
+        return f(FAKE, FAKE, B.size if R is None else R, B.ctypes.data, E, K, H, dtype, FAKE, FAKE, FAKE, FAKE, FAKE,
+                 FAKE, FAKE, None)
+
+    B = _B(3, 0, 5, 1)
+    assert call(B, R=0) == INVALID                                  # R = 0
+    assert call(_B(*([1] * 257)), E=257) == INVALID                 # R > 256
+    assert call(B, E=18) == INVALID                                 # E % R
+    assert call(B, K=17) == INVALID                                 # K > E
+    assert call(B, K=0) == INVALID
+    assert call(_B(3, -1, 5, 1)) == INVALID                         # negative B
+    assert call(_B(1 << 30, 1 << 30, 0, 0)) == INVALID              # T*K overflows int32
+    assert f(FAKE, FAKE, 4, None, 16, 2, 256, BF16, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == INVALID
+    # beyond the 1 MiB static scratch: 1024 experts, top-32, 8192 tokens
+    big = _B(8192)
+    assert lib.moe_dispatch_workspace_bytes(1, 1024, 32, 8192) > (1 << 20)
+    assert call(big, E=1024, K=32) == WORKSPACE
+    assert call(_B(4096, 4096), E=1024, K=32) == WORKSPACE
+
+
 def test_workspace_bytes(lib):
     f = lib.moe_dispatch_workspace_bytes
     assert f(0, 16, 2, 10) == 0 and f(4, 18, 2, 10) == 0 and f(4, 16, 0, 10) == 0 and f(4, 16, 2, -1) == 0
