@@ -134,3 +134,16 @@ def test_routing_load_shows_the_zipf_skew(oracle):
         assert load["rows_per_expert"]["mean"] * w.E == inp["T"] * w.K
         ratios[name] = load["rows_per_expert"]["max_over_mean"]
     assert ratios["toy"] < 2.0 < 10.0 < ratios["kimi_decode"]
+
+
+def test_gpu_arm_cpu_baseline_object(oracle):
+    # the GPU arm's cpu_baseline leg runs only the oracle, so it can be checked here
+    sys.path.insert(0, ROOT)
+    import bench
+    from combine_moe_route_gb300 import workloads as wl
+    T = int(wl.draw_B(wl.WORKLOADS["toy"], 0).sum())
+    cb = bench.cpu_baseline("toy", T)
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "us/layer" and cb["value"] > 0
+    assert "toy" in cb["sample"] and f"of {T}" in cb["sample"]
+    assert cb["host"]["nproc"] >= 1 and cb["host"]["model"]
+    json.dumps(cb)
