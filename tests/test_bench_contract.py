@@ -147,3 +147,23 @@ def test_gpu_arm_cpu_baseline_object(oracle):
     assert "toy" in cb["sample"] and f"of {T}" in cb["sample"]
     assert cb["host"]["nproc"] >= 1 and cb["host"]["model"]
     json.dumps(cb)
+
+
+def test_profile_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
+    # the roofline's traffic comes from a committed ncu summary, and only while the
+    # kernel source still has the hash recorded there
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    src_dir = tmp_path / "combine_moe_route_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (src_dir / "k.cu").write_text("__global__ void k() {}\n")
+    sha = hashlib.sha256((src_dir / "k.cu").read_bytes()).hexdigest()
+    (tmp_path / "profiles" / "k.md").write_text(
+        f"# k\n\n- dram_bytes_per_full_launch: 1234\n- kernel_source_sha256: {sha}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profile_traffic("k.cu", "k.md") == 1234.0
+    (src_dir / "k.cu").write_text("__global__ void k() { }\n")     # the kernel changed since the capture
+    assert bench.profile_traffic("k.cu", "k.md") is None
+    assert bench.profile_traffic("k.cu", "missing.md") is None
