@@ -167,3 +167,29 @@ def test_profile_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
     (src_dir / "k.cu").write_text("__global__ void k() { }\n")     # the kernel changed since the capture
     assert bench.profile_traffic("k.cu", "k.md") is None
     assert bench.profile_traffic("k.cu", "missing.md") is None
+
+
+def test_clock_summary_reads_the_timed_window():
+    # nvidia-smi rows (index, sm MHz, max sm MHz, power, hw_slowdown, hw_thermal,
+    # sw_thermal, sw_power_cap), stamped by arrival; only rows inside the timed
+    # region count, and a reason counts when it reads "Active"
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler(0)
+    rows = [(0.0, "0, 1200, 2070, 300.0, Not Active, Not Active, Not Active, Not Active"),    # warm-up
+            (1.0, "0, 2070, 2070, 900.0, Not Active, Not Active, Not Active, Active"),
+            (1.1, "0, 2055, 2070, 950.0, Not Active, Not Active, Not Active, Not Active"),
+            (1.2, "0, 2040, 2070, 990.0, Not Active, Not Active, Not Active, Active"),
+            (1.3, "[N/A], garbage"),
+            (9.0, "0, 900, 2070, 200.0, Active, Not Active, Not Active, Not Active")]         # after
+    c.lines = list(rows)
+    c.t_start, c.t_stop = 0.95, 1.25
+    got = c.summary()
+    assert got["sm_mhz"] == 2055.0 and got["sm_max_mhz"] == 2070.0 and got["samples"] == 3
+    assert got["reasons"] == ["sw_power_cap"] and got["window"] == "timed"
+    # a timed region shorter than the sampling period falls back to every row
+    c.t_start, c.t_stop = 5.0, 5.01
+    got = c.summary()
+    assert got["samples"] == 5 and "hw_slowdown" in got["reasons"] and got["window"].startswith("warmup")
+    c.lines = []
+    assert bench.ClockSampler(0).summary()["samples"] == 0
