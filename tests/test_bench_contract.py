@@ -2,7 +2,9 @@
 
 The GPU arm needs a GPU; what can be checked here is the reference arm (the
 CPU oracle timed on a sample of the workload), its behaviour under two ranks,
-and the algorithmic-byte accounting that the roofline fraction divides by."""
+and the GPU arm's host-side pieces: the algorithmic-byte accounting that the
+roofline fraction divides by, the ncu traffic lookup, the clock summary, the
+CPU-baseline object and the routing-load summary."""
 import json
 import os
 import socket
