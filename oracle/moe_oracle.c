@@ -226,10 +226,15 @@ void oracle_route_topk_grouped(const float *logits, int T, int E, int K, int n_g
 /* FP8 block quantisation of one token row: [DSD] "Quantization" (activation  */
 /* scales over 128-element vectors, computed on the fly) and [EPK] "Optimising */
 /* for latency" (FP8 payload for dispatch).  Reading: per block of 128        */
-/* channels, amax = max |x| (floored at 2^-64 so that 448/amax stays finite),  */
-/* scale = amax / 448 and inv = 448 / amax, each one IEEE fp32 division;       */
+/* channels, amax = max |x|, raised to at least 2^-119; scale = amax / 448 and */
+/* inv = 448 / amax, each one IEEE fp32 division (subnormal results kept);    */
 /* q = e4m3(x * inv) with one fp32 multiply and a saturating round-to-nearest- */
 /* even encode.  Dequantised value: e4m3_decode(q) * scale.                    */
+/* The pages say nothing of zero or tiny blocks.  2^-119 is the smallest power */
+/* of two for which 448 / amax is finite in fp32 (448 * 2^119 = 1.75 * 2^127); */
+/* below it the division would overflow and a zero element would give 0 * inf. */
+/* With this floor no nonzero bf16 value encodes to a zero code because of the */
+/* floor: the smallest, 2^-133, scales to 448 * 2^-14, above e4m3's 2^-6.      */
 /* ------------------------------------------------------------------------ */
 static void quantize_row_e4m3(const uint16_t *xrow, int H, uint8_t *q, float *scale)
 {
@@ -239,7 +244,7 @@ static void quantize_row_e4m3(const uint16_t *xrow, int H, uint8_t *q, float *sc
             float v = fabsf(oracle_f32_from_bf16(xrow[b * 128 + i]));
             if (v > amax) amax = v;
         }
-        if (amax < 0x1p-64f) amax = 0x1p-64f;
+        if (amax < 0x1p-119f) amax = 0x1p-119f;
         float s = amax / 448.0f;
         float inv = 448.0f / amax;
         scale[b] = s;

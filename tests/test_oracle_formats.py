@@ -127,7 +127,7 @@ def _torch_block_quant(x_bf16_bits):
     x = torch.from_numpy(x_bf16_bits.view(np.int16).copy()).view(torch.bfloat16).float()
     n, H = x.shape
     xb = x.view(n, H // 128, 128)
-    amax = xb.abs().amax(dim=-1, keepdim=True).clamp_min(2.0**-64)
+    amax = xb.abs().amax(dim=-1, keepdim=True).clamp_min(2.0**-119)
     c448 = torch.full_like(amax, 448.0)
     scale = amax / c448          # tensor / tensor: IEEE division (a scalar operand
     inv = c448 / amax            # would make torch multiply by a reciprocal instead)
@@ -140,7 +140,8 @@ def test_block_quant_matches_library_ops(oracle):
     rng = np.random.default_rng(5)
     x32 = rng.standard_normal((64, 1024)).astype(np.float32)
     x32[3, :128] = 0.0                            # an all-zero block
-    x32[4, 128:256] *= 1e-30                      # a tiny block (floor path not hit, amax > 2^-64)
+    x32[4, 128:256] *= 1e-30                      # a tiny block (amax above the 2^-119 floor)
+    x32[6, 512:640] *= 2.0**-140                  # below the floor: bf16 subnormals and zeros
     x32[5, 256:384] = 1e-25                       # constant block
     xb = oracle.bf16_from_f32(x32)
     q, s = oracle.quantize_rows_e4m3(xb)
@@ -164,3 +165,70 @@ def test_block_quant_error_bound_and_amax_code(oracle):
     e = np.floor(np.log2(np.maximum(p, 2.0**-6)))
     half = 0.5 * 2.0 ** (e - 3)
     assert np.all(np.abs(dq - x) <= (half * s[..., None]) * (1 + 1e-5) + 1e-30)
+
+
+# ---------------------------------------------------------------------------
+# blocks at and below the amax floor, in exact rational arithmetic
+# ---------------------------------------------------------------------------
+
+def _rn_f32(q):
+    """The float32 nearest to the rational q (ties to even), subnormals included."""
+    from fractions import Fraction
+    f = np.float32(float(q))
+    cands = [f, np.nextafter(f, np.float32(np.inf)), np.nextafter(f, np.float32(-np.inf))]
+    cands = [c for c in cands if np.isfinite(c)]
+    best = min(abs(Fraction(float(c)) - q) for c in cands)
+    near = [c for c in cands if abs(Fraction(float(c)) - q) == best]
+    near.sort(key=lambda c: int(np.array(c, np.float32).view(np.uint32)) & 1)   # even significand first
+    return np.float32(near[0])
+
+
+def _e4m3_nearest_code(p):
+    """The E4M3 code nearest to the rational p by brute force over the finite codes (ties
+    to the even significand; -0 for a negative value that rounds to zero)."""
+    from fractions import Fraction
+    best, best_code = None, None
+    for c in range(0x7F):                          # 0x00 .. 0x7E: +0 .. 448
+        e, m = c >> 3, c & 7
+        v = Fraction(m, 8) * Fraction(2) ** -6 if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+        d = abs(v - abs(p))
+        if best is None or d < best or (d == best and (c & 1) == 0):
+            best, best_code = d, c
+    return best_code | (0x80 if p < 0 else 0)
+
+
+TINY_AMAX = [0.0, 2.0**-70, 2.0**-100, 2.0**-119, float.fromhex("0x1.fep-120"), 2.0**-126, 2.0**-133]
+
+
+@pytest.mark.parametrize("amax", TINY_AMAX)
+def test_block_quant_tiny_blocks_exact(oracle, amax):
+    """Blocks whose largest magnitude is 0, 2^-70, 2^-100, 2^-119 (the floor), the bf16 value
+    just below it, 2^-126 and the smallest bf16 subnormal 2^-133.  The oracle's codes and
+    scale must equal the definition evaluated in exact arithmetic: amax raised to 2^-119,
+    scale = RN(amax/448), inv = RN(448/amax), code = the E4M3 value nearest to RN(x * inv).
+    Every nonzero bf16 input keeps a nonzero code, and zeros keep their sign."""
+    from fractions import Fraction
+    rng = np.random.default_rng(int(amax * 2.0**140) % 1000 + 7)
+    # 128 bf16 values in [-amax, amax], the largest magnitude exactly amax, with zeros of both signs
+    frac = rng.uniform(-1, 1, 128).astype(np.float32)
+    x = (frac * np.float32(amax)).astype(np.float32) if amax > 0 else np.zeros(128, np.float32)
+    xb = oracle.bf16_from_f32(x)
+    xb[5] = oracle.bf16_from_f32(np.array([amax], np.float32))[0]
+    xb[6] = 0x0000
+    xb[7] = 0x8000
+    v = oracle.f32_from_bf16(xb)
+    assert np.abs(v).max() == np.float32(amax)
+    q, s = oracle.quantize_rows_e4m3(xb.reshape(1, 128))
+    a = max(Fraction(float(amax)), Fraction(2) ** -119)
+    scale = _rn_f32(a / 448)
+    inv = _rn_f32(448 / a)
+    assert np.isfinite(inv)
+    assert int(s.view(np.uint32)[0, 0]) == int(np.array(scale, np.float32).view(np.uint32))
+    want = np.array([_e4m3_nearest_code(Fraction(float(_rn_f32(Fraction(float(vi)) * Fraction(float(inv))))))
+                     if vi != 0 else (0x80 if np.signbit(vi) else 0x00) for vi in v], np.uint8)
+    assert np.array_equal(q[0], want)
+    nz = v != 0
+    assert np.all((q[0][nz] & 0x7F) != 0)          # no nonzero input lost to a zero code
+    assert q[0][6] == 0x00 and q[0][7] == 0x80
+    if amax >= 2.0**-119:                            # at or above the floor: amax maps to 448
+        assert (q[0][5] & 0x7F) == 0x7E

@@ -165,6 +165,14 @@ MUTATIONS = [
      "acc = fmaf(topk_w[g * K + j], v, acc);",
      "acc = oracle_f32_from_bf16(oracle_bf16_from_f32(fmaf(topk_w[g * K + j], v, acc)));",
      [P.test_combine_fp32_within_error_bound_of_exact]),
+    ("FP8 amax floor at 2^-64 (tiny blocks quantise to zero codes)",
+     "if (amax < 0x1p-119f) amax = 0x1p-119f;",
+     "if (amax < 0x1p-64f) amax = 0x1p-64f;",
+     [F.test_block_quant_tiny_blocks_exact]),
+    ("FP8 amax floor one binade too high (2^-118)",
+     "if (amax < 0x1p-119f) amax = 0x1p-119f;",
+     "if (amax < 0x1p-118f) amax = 0x1p-118f;",
+     [F.test_block_quant_tiny_blocks_exact]),
     ("partial stored in the slot of the last copy on that rank",
      "if (j0 < 0) j0 = j;",
      "j0 = j;",
