@@ -246,67 +246,129 @@ def time_flushed(fn, stream, flush, reps: int = 50) -> float:
     return statistics.median(a.elapsed_time(z) for a, z in ev) * 1e3
 
 
-def measure_decode_layouts(dev, stream, flush):
-    """DeepSeek-V3 decode layer (R=8, E=256, K=8, H=7168, 128 tokens/rank, bf16): dispatch and
-    combine through the throughput (ragged) layout and through the low-latency rectangle
-    (chunk cap C = 128; slots in token order, or taken by atomic increments), each call timed on
-    its own with the L2 flushed."""
+def time_flushed_after(first, fn, stream, flush, reps: int = 50) -> float:
+    """Median µs of fn() when each call follows first() (L2 flushed before first(), outside
+    the events): for a receive half, which has something to receive only after its send."""
+    for _ in range(3):
+        first()
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    gc_was_on = gc.isenabled()
+    gc.disable()
+    try:
+        for a, z in ev:
+            flush.fill_(3)
+            first()
+            a.record(stream)
+            fn()
+            z.record(stream)
+        torch.cuda.synchronize()
+    finally:
+        if gc_was_on:
+            gc.enable()
+    return statistics.median(a.elapsed_time(z) for a, z in ev) * 1e3
+
+
+def measure_workload(name, dev, stream, flush, peak):
+    """One workload on its own (the benchmark line's headline is the prefill layer; this covers
+    every other one): T, dispatch and combine µs (flushed medians of 50 calls), their
+    algorithmic bytes, the fraction of the measured copy peak and the % of 8 TB/s, and the
+    CUDA-graph replay of dispatch + combine.  For the bf16 decode layers also the low-latency
+    rectangle (chunk cap C = the largest rank; slots in token order, by atomic increments, and
+    with the FP8 payload), its combine, and the graph replays of those forms."""
+    from combine_moe_route_gb300 import binding as b
+    from combine_moe_route_gb300 import workloads as wl
+    w = wl.WORKLOADS[name]
+    inp = wl.generate(w, seed=0)
+    B, T, E, K, H, R = inp["B"], inp["T"], w.E, w.K, w.H, w.R
+    x = inp["x"].to(dev)
+    logits = torch.from_numpy(inp["logits"]).to(dev)
+    idx, wts = b.route_topk(logits, K)
+    d = b.dispatch(x, idx, B, E, fp8=w.fp8)
+    y = b.expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E)
+    out = b.combine(y, d.tok2row, wts)
+    torch.cuda.synchronize()
+    db = dispatch_bytes(T, E, R, K, H, w.fp8)
+    cb = combine_bytes(T, K, H)
+    res = {"T": T, "R": R, "E": E, "K": K, "H": H, "payload": "fp8_e4m3" if w.fp8 else "bf16",
+           "route_us": time_flushed(lambda: b.route_topk(logits, K, topk_idx=idx, topk_w=wts), stream, flush),
+           "dispatch_us": time_flushed(lambda: b.dispatch(x, idx, B, E, fp8=w.fp8, out=d), stream, flush),
+           "combine_us": time_flushed(lambda: b.combine(y, d.tok2row, wts, out=out), stream, flush),
+           "algorithmic_bytes": {"dispatch": db, "combine": cb}}
+    res["dispatch_plus_combine_us"] = res["dispatch_us"] + res["combine_us"]
+    res["frac_of_measured_peak"] = {"dispatch": db / (res["dispatch_us"] * 1e-6) / 1e9 / peak,
+                                    "combine": cb / (res["combine_us"] * 1e-6) / 1e9 / peak}
+    res["pct_of_8TBs"] = {"dispatch": 100 * db / (res["dispatch_us"] * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
+                          "combine": 100 * cb / (res["combine_us"] * 1e-6) / 1e9 / NOMINAL_HBM_GBS}
+    res["floor_us_at_8TBs"] = {"dispatch": db / 8e6, "combine": cb / 8e6}
+    res["floor_us_at_measured_peak"] = {"dispatch": db / (peak * 1e3), "combine": cb / (peak * 1e3)}
+    graphs = []
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        b.dispatch(x, idx, B, E, fp8=w.fp8, out=d)
+        b.combine(y, d.tok2row, wts, out=out)
+    graphs.append(g)
+    torch.cuda.synchronize()
+    res["graph_dispatch_plus_combine_us"] = time_flushed(g.replay, stream, flush)
+    if not w.fp8:
+        C = max(1, int(B.max()))
+        eo = torch.arange(E + 1, dtype=torch.int32, device=dev) * (R * C)
+        dl = b.dispatch_ll(x, idx, B, E, C)
+        du = b.dispatch_ll(x, idx, B, E, C, unordered=True)
+        dl8 = b.dispatch_ll(x, idx, B, E, C, fp8=True)
+        du8 = b.dispatch_ll(x, idx, B, E, C, fp8=True, unordered=True)
+        yl = b.expert_scale(dl.recv_x, None, eo, E)
+        yu = b.expert_scale(du.recv_x, None, eo, E)
+        outl = b.combine_ll(yl, E, R, C, dl.tok2row, wts)
+        outu = b.combine_ll(yu, E, R, C, du.tok2row, wts)
+        torch.cuda.synchronize()
+        ll = {"C": C, "rectangle_rows": E * R * C,
+              "ordered_dispatch_us": time_flushed(lambda: b.dispatch_ll(x, idx, B, E, C, out=dl), stream, flush),
+              "unordered_dispatch_us": time_flushed(
+                  lambda: b.dispatch_ll(x, idx, B, E, C, unordered=True, out=du), stream, flush),
+              "ordered_fp8_dispatch_us": time_flushed(
+                  lambda: b.dispatch_ll(x, idx, B, E, C, fp8=True, out=dl8), stream, flush),
+              "unordered_fp8_dispatch_us": time_flushed(
+                  lambda: b.dispatch_ll(x, idx, B, E, C, fp8=True, unordered=True, out=du8), stream, flush),
+              "rectangle_combine_us": time_flushed(lambda: b.combine_ll(yl, E, R, C, dl.tok2row, wts, out=outl),
+                                                   stream, flush)}
+        gl = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gl):
+            b.dispatch_ll(x, idx, B, E, C, out=dl)
+            b.combine_ll(yl, E, R, C, dl.tok2row, wts, out=outl)
+        gu = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gu):
+            b.dispatch_ll(x, idx, B, E, C, unordered=True, out=du)
+            b.combine_ll(yu, E, R, C, du.tok2row, wts, out=outu)
+        graphs += [gl, gu]
+        torch.cuda.synchronize()
+        ll["graph_ordered_dispatch_plus_combine_us"] = time_flushed(gl.replay, stream, flush)
+        ll["graph_unordered_dispatch_plus_combine_us"] = time_flushed(gu.replay, stream, flush)
+        res["low_latency"] = ll
+    res["routing_load"] = routing_load(d.counts.cpu().numpy(), E, R)
+    del graphs
+    return _rounded(res)
+
+
+def _rounded(v):
+    if isinstance(v, float):
+        return round(v, 4)
+    if isinstance(v, dict):
+        return {k: _rounded(u) for k, u in v.items()}
+    return v
+
+
+def measure_eager_layers(dev, stream):
+    """Whole eager DeepSeek-V3 decode layers (route, dispatch, expert stand-in, combine) enqueued
+    back to back: through the package functions, whose per-call checks cost host time, and
+    through BoundLayer."""
     from combine_moe_route_gb300 import binding as b
     from combine_moe_route_gb300 import workloads as wl
     w = wl.WORKLOADS["dsv3_decode"]
     inp = wl.generate(w, seed=0)
-    B, T, E, K, H, C = inp["B"], inp["T"], w.E, w.K, w.H, int(inp["B"].max())
-    R = w.R
+    B, E, K = inp["B"], w.E, w.K
     x = inp["x"].to(dev)
-    idx, wts = b.route_topk(torch.from_numpy(inp["logits"]).to(dev), K)
-    d = b.dispatch(x, idx, B, E)
-    y = b.expert_scale(d.recv_x, None, d.expert_offsets, E)
-    out = b.combine(y, d.tok2row, wts)
-    dl = b.dispatch_ll(x, idx, B, E, C)
-    eo = torch.arange(E + 1, dtype=torch.int32, device=dev) * (R * C)
-    yl = b.expert_scale(dl.recv_x, None, eo, E)
-    outl = b.combine_ll(yl, E, R, C, dl.tok2row, wts)
-    ret = b.combine_ll_push(yl, dl, R, E, T, K)
-    du = b.dispatch_ll(x, idx, B, E, C, unordered=True)      # slots by atomic increments, no histogram
-    dl8 = b.dispatch_ll(x, idx, B, E, C, fp8=True)           # the FP8 payload the sources send by default
-    du8 = b.dispatch_ll(x, idx, B, E, C, fp8=True, unordered=True)
-    yu = b.expert_scale(du.recv_x, None, eo, E)
-    outu = b.combine_ll(yu, E, R, C, du.tok2row, wts)
-    torch.cuda.synchronize()
-    res = {
-        "ragged_dispatch_us": time_flushed(lambda: b.dispatch(x, idx, B, E, out=d), stream, flush),
-        "ragged_combine_us": time_flushed(lambda: b.combine(y, d.tok2row, wts, out=out), stream, flush),
-        "ll_dispatch_us": time_flushed(lambda: b.dispatch_ll(x, idx, B, E, C, out=dl), stream, flush),
-        "ll_unordered_dispatch_us": time_flushed(
-            lambda: b.dispatch_ll(x, idx, B, E, C, unordered=True, out=du), stream, flush),
-        "ll_fp8_dispatch_us": time_flushed(lambda: b.dispatch_ll(x, idx, B, E, C, fp8=True, out=dl8), stream, flush),
-        "ll_unordered_fp8_dispatch_us": time_flushed(
-            lambda: b.dispatch_ll(x, idx, B, E, C, fp8=True, unordered=True, out=du8), stream, flush),
-        "ll_combine_gather_us": time_flushed(lambda: b.combine_ll(yl, E, R, C, dl.tok2row, wts, out=outl),
-                                             stream, flush),
-        "ll_combine_push_us": time_flushed(lambda: b.combine_ll_push(yl, dl, R, E, T, K, out=ret), stream, flush),
-        "ll_combine_reduce_us": time_flushed(lambda: b.combine(ret, None, wts, out=outl), stream, flush),
-    }
-    # CUDA-graph replay of dispatch + combine (one graph per batch size, as the sources deploy it);
-    # the graph is replayed back to back, L2 flushed before each replay outside the events
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        b.dispatch(x, idx, B, E, out=d)
-        b.combine(y, d.tok2row, wts, out=out)
-    gl = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gl):
-        b.dispatch_ll(x, idx, B, E, C, out=dl)
-        b.combine_ll(yl, E, R, C, dl.tok2row, wts, out=outl)
-    gu = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gu):
-        b.dispatch_ll(x, idx, B, E, C, unordered=True, out=du)
-        b.combine_ll(yu, E, R, C, du.tok2row, wts, out=outu)
-    torch.cuda.synchronize()
-    res["graph_ragged_dispatch_plus_combine_us"] = time_flushed(g.replay, stream, flush)
-    res["graph_ll_dispatch_plus_combine_us"] = time_flushed(gl.replay, stream, flush)
-    res["graph_ll_unordered_dispatch_plus_combine_us"] = time_flushed(gu.replay, stream, flush)
-    # whole eager decode layers (route, dispatch, expert stand-in, combine) enqueued back to back:
-    # through the package functions, whose per-call checks cost host time, and through BoundLayer
     logits = torch.from_numpy(inp["logits"]).to(dev)
     bound = b.BoundLayer(x, logits, B, E, K)
 
@@ -322,12 +384,99 @@ def measure_decode_layouts(dev, stream, flush):
         torch.cuda.synchronize()
         return a.elapsed_time(z) * 1e3 / n
 
-    res["eager_layer_package_us"] = eager_us(lambda: b.moe_layer(x, logits, B, E, K))
-    res["eager_layer_bound_us"] = eager_us(bound)
-    db = dispatch_bytes(T, E, R, K, H, False)
-    cb = combine_bytes(T, K, H)
-    res["floor_us_at_8TBs"] = {"dispatch": db / 8e6, "combine": cb / 8e6}
-    return {"dsv3_decode_layouts": {k: (round(v, 2) if isinstance(v, float) else v) for k, v in res.items()}}
+    return {"eager_dsv3_decode_layer": {"package_us": round(eager_us(lambda: b.moe_layer(x, logits, B, E, K)), 2),
+                                        "bound_us": round(eager_us(bound), 2)}}
+
+
+def measure_split_halves(name, dev, stream, flush, inter=2048, reps=20):
+    """The split dispatch and combine on one workload: each half timed alone (flushed medians),
+    against the one-call forms; then Dispatch Overlap ([DSD] "Computation and communication
+    overlap"): the send half on a side stream while a dummy shared expert -- silu(x W1) W2,
+    bf16 cuBLAS GEMMs of intermediate size `inter` -- runs on the main stream, then the receive
+    half behind an event.  The send half is given every SM or a capped budget, so that the
+    shared expert keeps the rest.  Reported per budget: serialised (one stream) and overlapped
+    µs, and the fraction of the dispatch hidden."""
+    from combine_moe_route_gb300 import binding as b
+    from combine_moe_route_gb300 import workloads as wl
+    w = wl.WORKLOADS[name]
+    inp = wl.generate(w, seed=0)
+    B, T, E, K, H, R = inp["B"], inp["T"], w.E, w.K, w.H, w.R
+    x = inp["x"].to(dev)
+    idx, wts = b.route_topk(torch.from_numpy(inp["logits"]).to(dev), K)
+    d = b.dispatch(x, idx, B, E, fp8=w.fp8)
+    ds = b.dispatch_send(x, idx, B, E, fp8=w.fp8)
+    b.dispatch_recv(ds, B, E, K)
+    y = b.expert_scale(ds.recv_x, ds.recv_scale, ds.expert_offsets, E)
+    out = b.combine(y, ds.tok2row, wts)
+    torch.cuda.synchronize()
+    res = {"T": T,
+           "dispatch_us": time_flushed(lambda: b.dispatch(x, idx, B, E, fp8=w.fp8, out=d), stream, flush),
+           "dispatch_send_us": time_flushed(lambda: b.dispatch_send(x, idx, B, E, fp8=w.fp8, out=ds), stream, flush),
+           "dispatch_recv_us": time_flushed_after(lambda: b.dispatch_send(x, idx, B, E, fp8=w.fp8, out=ds),
+                                                  lambda: b.dispatch_recv(ds, B, E, K), stream, flush),
+           "dispatch_send_plus_recv_us": time_flushed(
+               lambda: (b.dispatch_send(x, idx, B, E, fp8=w.fp8, out=ds), b.dispatch_recv(ds, B, E, K)),
+               stream, flush),
+           "combine_us": time_flushed(lambda: b.combine(y, ds.tok2row, wts, out=out), stream, flush),
+           "combine_send_plus_recv_us": time_flushed(
+               lambda: (b.combine_send(ds.workspace, R), b.combine_recv(y, ds.tok2row, wts, ds.workspace, R, out=out)),
+               stream, flush)}
+    st, code = b.get_device_error(ds.workspace)
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x} in the split halves")
+
+    gen = torch.Generator(device=dev).manual_seed(0)
+    w1 = (torch.randn((H, inter), device=dev, generator=gen) * H ** -0.5).to(torch.bfloat16)
+    w2 = (torch.randn((inter, H), device=dev, generator=gen) * inter ** -0.5).to(torch.bfloat16)
+    side = torch.cuda.Stream(dev)
+
+    def shared():
+        return torch.nn.functional.silu(x @ w1) @ w2
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(4)
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            z.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(z) * 1e3)
+        return statistics.median(ts)
+
+    res["shared_expert_us"] = timed(shared)
+    overlap = {}
+    for max_sms in (0, 114, 76):
+        def serial():
+            b.dispatch_send(x, idx, B, E, fp8=w.fp8, max_sms=max_sms, out=ds)
+            shared()
+            b.dispatch_recv(ds, B, E, K)
+
+        def overlapped():
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                b.dispatch_send(x, idx, B, E, fp8=w.fp8, max_sms=max_sms, out=ds)
+                sent = torch.cuda.Event()
+                sent.record(side)
+            shared()
+            stream.wait_event(sent)
+            b.dispatch_recv(ds, B, E, K)
+
+        send_alone = timed(lambda: b.dispatch_send(x, idx, B, E, fp8=w.fp8, max_sms=max_sms, out=ds))
+        ser, ovl = timed(serial), timed(overlapped)
+        overlap[f"max_sms_{max_sms or 'all'}"] = {
+            "send_alone_us": send_alone, "serialised_us": ser, "overlapped_us": ovl,
+            "hidden_frac_of_dispatch": (ser - ovl) / res["dispatch_us"]}
+    res["dispatch_overlap"] = overlap
+    st, code = b.get_device_error(ds.workspace)
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x} in the overlap runs")
+    return _rounded(res)
 
 
 def measure_partial_combine(b, y, d, idx, wts, out, E, R, K, H, T, stream, flush):
@@ -360,55 +509,6 @@ def measure_partial_combine(b, y, d, idx, wts, out, E, R, K, H, T, stream, flush
         "rows_returned": distinct, "rows_returned_receive_side": T * K,
         "return_bytes_saved_frac": round(1.0 - distinct / (T * K), 4),
         "error_vs_fp64": errs}}
-
-
-def measure_dispatch_overlap(b, x, idx, B, E, fp8, d, H, stream, flush, inter=2048, reps=20):
-    """Dispatch overlapped with a dummy shared expert (the pages' "Dispatch Overlap": the
-    shared expert runs while dispatch moves tokens).  The shared expert stand-in is
-    silu(x W1) W2 with bf16 cuBLAS GEMMs (intermediate size `inter`), on a second stream;
-    reported: each alone, both serialised on one stream, and both on two streams."""
-    gen = torch.Generator(device=x.device).manual_seed(0)
-    w1 = (torch.randn((H, inter), device=x.device, generator=gen) * H ** -0.5).to(torch.bfloat16)
-    w2 = (torch.randn((inter, H), device=x.device, generator=gen) * inter ** -0.5).to(torch.bfloat16)
-    side = torch.cuda.Stream(x.device)
-
-    def shared():
-        return torch.nn.functional.silu(x @ w1) @ w2
-
-    def disp():
-        b.dispatch(x, idx, B, E, fp8=fp8, out=d)
-
-    def timed(fn):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(reps):
-            flush.fill_(4)
-            a = torch.cuda.Event(enable_timing=True)
-            z = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            z.record(stream)
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(z) * 1e3)
-        return statistics.median(ts)
-
-    def both_serial():
-        disp()
-        shared()
-
-    def both_overlapped():
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            disp()
-        shared()
-        stream.wait_stream(side)
-
-    res = {"dispatch_us": timed(disp), "shared_expert_us": timed(shared),
-           "serialised_us": timed(both_serial), "overlapped_us": timed(both_overlapped)}
-    res["hidden_frac_of_dispatch"] = (res["serialised_us"] - res["overlapped_us"]) / res["dispatch_us"]
-    return {"dispatch_overlap": {k: round(v, 3) for k, v in res.items()}}
 
 
 def replica_value(per_rank_us: float, world: int) -> float:
@@ -460,18 +560,47 @@ def pct(ms: list) -> list:
 
 
 def host_cpu() -> dict:
-    """The host's logical CPU count and model name (from /proc/cpuinfo where it has one)."""
-    model = platform.processor() or platform.machine()
+    """The host's logical CPU count and model: lscpu's "Model name" (on Arm hosts lscpu names
+    the core, e.g. Neoverse-V2, where /proc/cpuinfo has no model line), else /proc/cpuinfo;
+    on Arm also the main ID register (implementer 0x41 = Arm; part 0xd4f = Neoverse V2)."""
+    model = None
     try:
-        with open("/proc/cpuinfo") as f:
-            for line in f:
-                key = line.split(":", 1)[0].strip().lower()
-                if key in ("model name", "cpu model", "hardware"):
-                    model = line.split(":", 1)[1].strip()
-                    break
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":", 1)[0].strip().lower() == "model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    key = line.split(":", 1)[0].strip().lower()
+                    if key in ("model name", "cpu model", "hardware"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    info = {"nproc": os.cpu_count(), "model": model or platform.processor() or platform.machine(),
+            "machine": platform.machine()}
+    try:
+        with open("/sys/devices/system/cpu/cpu0/regs/identification/midr_el1") as f:
+            info["midr_el1"] = f.read().strip()
     except OSError:
         pass
-    return {"nproc": os.cpu_count(), "model": model}
+    return info
+
+
+def path_dtype(w) -> str:
+    """The arithmetic types the path computes in, for the bench line's ``dtype``."""
+    if w.fp8:
+        return "e4m3 dispatch payload + f32 scale per 128 channels; bf16 rows; f32 accumulate"
+    return "bf16 rows; f32 accumulate"
+
+
+L2_NOTE = (f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write before route, dispatch and combine "
+           "(outside their events)")
 
 
 def cpu_baseline(workload: str, T_full: int):
@@ -514,8 +643,8 @@ def run_reference(args, world, rank):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps),
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": bench_config(w, T_full, "CPU oracle"),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": path_dtype(w),
+        "data": "synthetic", "config": bench_config(w, T_full, L2_NOTE),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "host": host_cpu(),
                          "sample": f"{args.workload} with {tpr} tokens/rank per step (T={inp['T']} of {T_full}), "
                                    "oracle dispatch + combine scaled by T_full/T_sample; single-threaded C"},
@@ -696,9 +825,22 @@ def run_ours(args, world, rank, local):
         us = time_call(grouped, stream, reps=50)
         next_rows["route_grouped_G8_M4"] = {"us": us, "GBps": route_bytes(T, E, K) / (us * 1e-6) / 1e9}
 
-    next_rows.update(measure_decode_layouts(dev, stream, flush))
     next_rows.update(measure_partial_combine(b, y, d, idx, wts, out, E, w.R, K, H, T, stream, flush))
-    next_rows.update(measure_dispatch_overlap(b, x, idx, B, E, w.fp8, d, H, stream, flush))
+    next_rows.update(measure_eager_layers(dev, stream))
+    peak_gbs, _ = measured_peaks()
+    split = {}
+    if args.tokens_per_rank is None:
+        split[args.workload] = measure_split_halves(args.workload, dev, stream, flush)
+        if args.workload != "dsv3_decode":
+            split["dsv3_decode"] = measure_split_halves("dsv3_decode", dev, stream, flush)
+    next_rows["split_halves"] = split
+    # every other workload, each on its own (parity cases of the same path, not the headline)
+    others = {}
+    if args.tokens_per_rank is None and not args.headline_only:
+        for name in ("toy", "dsv3_decode", "kimi_decode", "wide_ep_decode", "dsv3_prefill"):
+            if name != args.workload:
+                others[name] = measure_workload(name, dev, stream, flush, peak_gbs)
+                torch.cuda.empty_cache()
 
     # correctness of what was timed: the last step's outputs equal the first layer's
     st, code = b.get_device_error(d.workspace)
@@ -741,10 +883,9 @@ def run_ours(args, world, rank, local):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": path_dtype(w),
         "data": "synthetic (seeded N(0,1) tokens and router logits, see combine_moe_route_gb300/workloads.py)",
-        "config": bench_config(w, T, f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write before route, dispatch and "
-                                     "combine (outside their events)", args.tokens_per_rank),
+        "config": bench_config(w, T, L2_NOTE, args.tokens_per_rank),
         "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} (hbm_gbs)", "unit": "GB/s", "frac": achieved / peak,
                      "traffic": dom["traffic"], "algorithmic_bytes": dom["bytes"]},
@@ -769,6 +910,7 @@ def run_ours(args, world, rank, local):
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"], "window": clk["window"]},
         "cpu_baseline": cpu,
+        "workloads": others,
         "next_rows": next_rows,
     }
     if line_note:
@@ -784,6 +926,8 @@ def main():
     p.add_argument("--workload", default="dsv3_prefill")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--headline-only", action="store_true",
+                   help="skip the per-workload measurements of the other four layers")
     p.add_argument("--tokens-per-rank", type=int, default=None,
                    help="override B (every rank) for a smaller case of the workload, e.g. for ncu captures")
     args = p.parse_args()

@@ -39,13 +39,18 @@ def library_path() -> str:
     return _build.library_path()
 
 
-def load_library() -> ctypes.CDLL:
-    """Load libmoeroute.so (raises ImportError if it has not been built)."""
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libmoeroute.so (raises ImportError if it has not been built).
+
+    ``path`` loads another build of the library (one built with other tuning
+    defines, say) and returns it with its signatures declared, without making it
+    the one the functions below call."""
     global _lib
     with _lock:
-        if _lib is not None:
+        if path is None and _lib is not None:
             return _lib
-        path = library_path()
+        default = path is None
+        path = path or library_path()
         if not os.path.exists(path):
             raise ImportError(
                 f"libmoeroute.so not found at {path}; build it with "
@@ -81,9 +86,20 @@ def load_library() -> ctypes.CDLL:
         lib.moe_combine_partial_send.restype = i32
         lib.moe_combine_partial_recv.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
         lib.moe_combine_partial_recv.restype = i32
+        lib.moe_dispatch_send.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, i32, vp, sz, vp]
+        lib.moe_dispatch_send.restype = i32
+        lib.moe_dispatch_recv.argtypes = [i32, vp, i32, i32, vp, vp, vp, vp, sz, vp]
+        lib.moe_dispatch_recv.restype = i32
+        lib.moe_combine_send.argtypes = [i32, vp, sz, vp]
+        lib.moe_combine_send.restype = i32
+        lib.moe_combine_recv.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, i32, vp, sz, vp]
+        lib.moe_combine_recv.restype = i32
         lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
         lib.moe_get_device_error.restype = i32
-        _lib = lib
+        lib.moe_dispatch_noalloc.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.moe_dispatch_noalloc.restype = i32
+        if default:
+            _lib = lib
         return lib
 
 
@@ -519,6 +535,113 @@ class BoundLayer:
 
 
 # ---------------------------------------------------------------------------
+# split dispatch and combine (send and receive halves)
+# ---------------------------------------------------------------------------
+
+def _dispatch_buffers(T: int, H: int, E: int, R: int, K: int, fp8: bool, dev) -> DispatchResult:
+    rows = T * K
+    return DispatchResult(
+        recv_x=torch.empty((rows, H), dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16, device=dev),
+        recv_scale=torch.empty((rows, H // 128), dtype=torch.float32, device=dev) if fp8 else None,
+        counts=torch.empty(E * R, dtype=torch.int32, device=dev),
+        offsets=torch.empty(E * R + 1, dtype=torch.int32, device=dev),
+        expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+        tok2row=torch.empty(rows, dtype=torch.int32, device=dev),
+        row2src=torch.empty(rows, dtype=torch.int32, device=dev),
+        workspace=torch.empty(max(dispatch_workspace_bytes(R, E, K, T), 256), dtype=torch.uint8, device=dev))
+
+
+def dispatch_send(x: torch.Tensor, topk_idx: torch.Tensor, B, E: int, *, fp8: bool = False, max_sms: int = 0,
+                  out: DispatchResult | None = None, stream=None) -> DispatchResult:
+    """Send half of the split dispatch: the rows, tok2row and row2src of ``dispatch``, each copy
+    announced to its destination rank.  ``counts``, ``offsets`` and ``expert_offsets`` of the
+    result are written by ``dispatch_recv``.  ``max_sms`` > 0 keeps the copy kernel on at most
+    that many SMs."""
+    _dev(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise ValueError("x must be [T, H]")
+    T, H = x.shape
+    _dev(topk_idx, "topk_idx", torch.int32)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != T:
+        raise ValueError("topk_idx must be [T, K]")
+    K = topk_idx.shape[1]
+    Bh = _host_B(B)
+    R = Bh.size
+    if int(Bh.astype(np.int64).sum()) != T:
+        raise ValueError(f"sum(B) = {int(Bh.sum())} does not match x.shape[0] = {T}")
+    dev = x.device
+    rows = T * K
+    if out is None:
+        out = _dispatch_buffers(T, H, E, R, K, fp8, dev)
+    _dev(out.recv_x, "recv_x", (torch.float8_e4m3fn, torch.uint8) if fp8 else torch.bfloat16, (rows, H))
+    if fp8:
+        _dev(out.recv_scale, "recv_scale", torch.float32, (rows, H // 128))
+    for name in ("tok2row", "row2src"):
+        _dev(getattr(out, name), name, torch.int32, (rows,))
+    _dev(out.workspace, "workspace", torch.uint8)
+    with torch.cuda.device(dev):
+        _check(load_library().moe_dispatch_send(
+            _ptr(x), _ptr(topk_idx), R, Bh.ctypes.data, E, K, H, _DTYPE_FP8 if fp8 else _DTYPE_BF16,
+            _ptr(out.recv_x), _ptr(out.recv_scale) if fp8 else None, _ptr(out.tok2row), _ptr(out.row2src),
+            int(max_sms), _ptr(out.workspace), out.workspace.numel(), _stream_handle(stream, dev)),
+            "moe_dispatch_send")
+    return out
+
+
+def dispatch_recv(d: DispatchResult, B, E: int, K: int, *, stream=None) -> DispatchResult:
+    """Receive half of the split dispatch: waits until the send half's copies have landed and
+    writes ``d.counts``, ``d.offsets`` and ``d.expert_offsets``."""
+    Bh = _host_B(B)
+    R = Bh.size
+    for name, n in (("counts", E * R), ("offsets", E * R + 1), ("expert_offsets", E + 1)):
+        _dev(getattr(d, name), name, torch.int32, (n,))
+    _dev(d.workspace, "workspace", torch.uint8)
+    dev = d.workspace.device
+    with torch.cuda.device(dev):
+        _check(load_library().moe_dispatch_recv(
+            R, Bh.ctypes.data, E, K, _ptr(d.counts), _ptr(d.offsets), _ptr(d.expert_offsets), _ptr(d.workspace),
+            d.workspace.numel(), _stream_handle(stream, dev)), "moe_dispatch_recv")
+    return d
+
+
+def combine_send(workspace: torch.Tensor, R: int, *, stream=None) -> None:
+    """Send half of the split combine: the expert ranks publish their outputs (enqueue it after
+    the work that wrote them)."""
+    _dev(workspace, "workspace", torch.uint8)
+    with torch.cuda.device(workspace.device):
+        _check(load_library().moe_combine_send(R, _ptr(workspace), workspace.numel(),
+                                               _stream_handle(stream, workspace.device)), "moe_combine_send")
+
+
+def combine_recv(y: torch.Tensor, tok2row: torch.Tensor, topk_w: torch.Tensor, workspace: torch.Tensor, R: int, *,
+                 out_dtype: torch.dtype = torch.bfloat16, out: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """Receive half of the split combine: waits for every expert rank's outputs, then the
+    weighted sum of ``combine`` -> [T, H]."""
+    _dev(y, "y", torch.bfloat16)
+    _dev(topk_w, "topk_w", torch.float32)
+    _dev(tok2row, "tok2row", torch.int32)
+    _dev(workspace, "workspace", torch.uint8)
+    if topk_w.dim() != 2:
+        raise ValueError("topk_w must be [T, K]")
+    T, K = topk_w.shape
+    H = y.shape[1]
+    if tok2row.numel() != T * K:
+        raise ValueError("tok2row must have T*K entries")
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype must be bfloat16 or float32")
+    if out is None:
+        out = torch.empty((T, H), dtype=out_dtype, device=y.device)
+    _dev(out, "out", out_dtype, (T, H))
+    with torch.cuda.device(y.device):
+        _check(load_library().moe_combine_recv(
+            _ptr(y), _ptr(tok2row), _ptr(topk_w), T, K, H,
+            _DTYPE_FP32 if out_dtype == torch.float32 else _DTYPE_BF16, _ptr(out), R, _ptr(workspace),
+            workspace.numel(), _stream_handle(stream, y.device)), "moe_combine_recv")
+    return out
+
+
+# ---------------------------------------------------------------------------
 # dispatch without a caller-supplied workspace
 # ---------------------------------------------------------------------------
 
@@ -529,11 +652,7 @@ def dispatch_noalloc(x: torch.Tensor, topk_idx: torch.Tensor, B, E: int, *, fp8:
     Every output buffer must be passed in ``out`` (its ``workspace`` is ignored);
     nothing is allocated here.  The first call on a device must come before any
     stream capture; calls that overlap on the GPU race on the shared scratch."""
-    lib = load_library()
-    fn = lib.moe_dispatch_noalloc
-    vp, i32 = ctypes.c_void_p, ctypes.c_int
-    fn.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
-    fn.restype = i32
+    fn = load_library().moe_dispatch_noalloc
     _dev(x, "x", torch.bfloat16)
     T, H = x.shape
     _dev(topk_idx, "topk_idx", torch.int32)

@@ -42,6 +42,33 @@ bool build_rank_table(int R, const int32_t *B, int K, moe::RankTable &rt, long l
 
 }  // namespace
 
+namespace moe {
+
+// The checks moe_dispatch makes before it looks at the workspace, in its
+// order.  On MOE_OK, rt, T and fp8 are filled; when T == 0 nothing is to be
+// scattered, and x, topk_idx and the payload and map pointers are not checked.
+// with_layout: the call writes counts / offsets / expert_offsets (moe_dispatch),
+// or leaves them to a receive half (moe_dispatch_send).
+moe_status check_dispatch_args(const void *x, const int32_t *topk_idx, int R, const int32_t *B, int E, int K, int H,
+                               moe_dtype recv_dtype, const void *recv_x, const float *recv_scale, bool with_layout,
+                               const int32_t *counts, const int32_t *offsets, const int32_t *expert_offsets,
+                               const int32_t *tok2row, const int32_t *row2src, RankTable &rt, long long &T,
+                               bool &fp8) {
+    if (R < 1 || R > MOE_MAX_RANKS || !B || !topk_shape_ok(E, K) || E % R != 0) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (recv_dtype != MOE_DTYPE_BF16 && recv_dtype != MOE_DTYPE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
+    fp8 = recv_dtype == MOE_DTYPE_FP8_E4M3;
+    if (fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (!build_rank_table(R, B, K, rt, T)) return MOE_ERR_INVALID_ARG;
+    if (with_layout && (!counts || !offsets || !expert_offsets)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !topk_idx || !recv_x || !tok2row || !row2src || (fp8 && !recv_scale)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(recv_x) || (fp8 && !aligned16(recv_scale))) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+}  // namespace moe
+
 extern "C" {
 
 int moe_abi_version(void) { return MOE_ROUTE_ABI_VERSION; }
@@ -84,18 +111,55 @@ size_t moe_dispatch_workspace_bytes(int R, int E, int K, int64_t T) {
     if (R < 1 || R > MOE_MAX_RANKS || !topk_shape_ok(E, K) || E % R != 0) return 0;
     if (T < 0 || T * K >= (1ll << 31)) return 0;
     const int ntiles = moe::max_tiles(R, K, T);
-    return moe::plan_dispatch(E, ntiles).total;
+    return moe::plan_dispatch(E, R, ntiles).total;
 }
 
 moe_status moe_dispatch(const void *x, const int32_t *topk_idx, int R, const int32_t *B, int E, int K, int H,
                         moe_dtype recv_dtype, void *recv_x, float *recv_scale, int32_t *counts, int32_t *offsets,
                         int32_t *expert_offsets, int32_t *tok2row, int32_t *row2src, void *workspace,
                         size_t workspace_bytes, moe_stream_t stream) {
+    moe::RankTable rt;
+    long long T = 0;
+    bool fp8 = false;
+    const moe_status v = moe::check_dispatch_args(x, topk_idx, R, B, E, K, H, recv_dtype, recv_x, recv_scale, true,
+                                                  counts, offsets, expert_offsets, tok2row, row2src, rt, T, fp8);
+    if (v != MOE_OK) return v;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E * R, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * ((size_t)E * R + 1), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * ((size_t)E + 1), st);
+        return cuda_status(e);
+    }
+    if (!workspace) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < moe::call_plan(rt, E, K).total) return MOE_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(moe::launch_dispatch(x, topk_idx, rt, E, K, H, fp8, recv_x, fp8 ? recv_scale : nullptr, counts,
+                                            offsets, expert_offsets, tok2row, row2src, workspace, st));
+}
+
+moe_status moe_dispatch_send(const void *x, const int32_t *topk_idx, int R, const int32_t *B, int E, int K, int H,
+                             moe_dtype recv_dtype, void *recv_x, float *recv_scale, int32_t *tok2row,
+                             int32_t *row2src, int max_sms, void *workspace, size_t workspace_bytes,
+                             moe_stream_t stream) {
+    moe::RankTable rt;
+    long long T = 0;
+    bool fp8 = false;
+    const moe_status v = moe::check_dispatch_args(x, topk_idx, R, B, E, K, H, recv_dtype, recv_x, recv_scale, false,
+                                                  nullptr, nullptr, nullptr, tok2row, row2src, rt, T, fp8);
+    if (v != MOE_OK) return v;
+    if (max_sms < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;   // nothing to send; the receive half writes the empty layout
+    if (!workspace) return MOE_ERR_WORKSPACE;
+    if (workspace_bytes < moe::call_plan(rt, E, K).total) return MOE_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(moe::launch_dispatch_send(x, topk_idx, rt, E, K, H, fp8, recv_x, fp8 ? recv_scale : nullptr,
+                                                 tok2row, row2src, workspace, max_sms, (cudaStream_t)stream));
+}
+
+moe_status moe_dispatch_recv(int R, const int32_t *B, int E, int K, int32_t *counts, int32_t *offsets,
+                             int32_t *expert_offsets, void *workspace, size_t workspace_bytes, moe_stream_t stream) {
     if (R < 1 || R > MOE_MAX_RANKS || !B || !topk_shape_ok(E, K) || E % R != 0) return MOE_ERR_INVALID_ARG;
-    if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0) return MOE_ERR_INVALID_ARG;
-    if (recv_dtype != MOE_DTYPE_BF16 && recv_dtype != MOE_DTYPE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
-    const bool fp8 = recv_dtype == MOE_DTYPE_FP8_E4M3;
-    if (fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
     moe::RankTable rt;
     long long T = 0;
     if (!build_rank_table(R, B, K, rt, T)) return MOE_ERR_INVALID_ARG;
@@ -107,14 +171,33 @@ moe_status moe_dispatch(const void *x, const int32_t *topk_idx, int R, const int
         if (e == cudaSuccess) e = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * ((size_t)E + 1), st);
         return cuda_status(e);
     }
-    if (!x || !topk_idx || !recv_x || !tok2row || !row2src || (fp8 && !recv_scale)) return MOE_ERR_INVALID_ARG;
     if (!workspace) return MOE_ERR_WORKSPACE;
-    const moe::DispatchPlan plan = moe::plan_dispatch(E, rt.ntiles);
-    if (workspace_bytes < plan.total) return MOE_ERR_WORKSPACE;
-    if (!aligned16(x) || !aligned16(recv_x) || !aligned16(workspace) || (fp8 && !aligned16(recv_scale)))
-        return MOE_ERR_UNSUPPORTED;
-    return cuda_status(moe::launch_dispatch(x, topk_idx, rt, E, K, H, fp8, recv_x, fp8 ? recv_scale : nullptr, counts,
-                                            offsets, expert_offsets, tok2row, row2src, workspace, st));
+    if (workspace_bytes < moe::call_plan(rt, E, K).total) return MOE_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(moe::launch_dispatch_recv(rt, E, K, counts, offsets, expert_offsets, workspace, st));
+}
+
+moe_status moe_combine_send(int R, void *workspace, size_t workspace_bytes, moe_stream_t stream) {
+    if (R < 1 || R > MOE_MAX_RANKS) return MOE_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < moe::signal_workspace_bytes(R)) return MOE_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(moe::launch_combine_send(R, workspace, (cudaStream_t)stream));
+}
+
+moe_status moe_combine_recv(const void *y, const int32_t *tok2row, const float *topk_w, int T, int K, int H,
+                            moe_dtype out_dtype, void *out, int R, void *workspace, size_t workspace_bytes,
+                            moe_stream_t stream) {
+    if (T < 0 || K < 1 || K > MOE_MAX_TOPK || R < 1 || R > MOE_MAX_RANKS) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H > MOE_MAX_HIDDEN || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * K >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+    if (out_dtype != MOE_DTYPE_BF16 && out_dtype != MOE_DTYPE_FP32) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y || !tok2row || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < moe::signal_workspace_bytes(R)) return MOE_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(moe::launch_combine_recv(y, tok2row, topk_w, T, K, H, out_dtype == MOE_DTYPE_FP32, out, R,
+                                                workspace, (cudaStream_t)stream));
 }
 
 moe_status moe_expert_scale(const void *recv_x, const float *recv_scale, moe_dtype recv_dtype,
@@ -170,7 +253,7 @@ static moe_status check_dispatch_ll(bool ordered, const void *x, const int32_t *
     if (T == 0) return cuda_status(cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E * R, st));
     if (!x || !topk_idx || !recv_x || !tok2row || !row2src || (fp8 && !recv_scale)) return MOE_ERR_INVALID_ARG;
     if (!workspace) return MOE_ERR_WORKSPACE;
-    const size_t need = ordered ? moe::plan_dispatch(E, rt.ntiles).total : moe::kWsHeader;
+    const size_t need = ordered ? moe::plan_dispatch(E, R, rt.ntiles).total : moe::kWsHeader;
     if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
     if (!aligned16(x) || !aligned16(recv_x) || !aligned16(workspace) || (fp8 && !aligned16(recv_scale)))
         return MOE_ERR_UNSUPPORTED;
@@ -263,7 +346,7 @@ moe_status moe_get_device_error(const void *workspace, int32_t *host_code, moe_s
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     *host_code = v;
-    if (v & (MOE_DEVERR_SCAN_TIMEOUT | MOE_DEVERR_COPY_TIMEOUT)) return MOE_ERR_TIMEOUT;
+    if (v & (MOE_DEVERR_SCAN_TIMEOUT | MOE_DEVERR_COPY_TIMEOUT | MOE_DEVERR_RECV_TIMEOUT)) return MOE_ERR_TIMEOUT;
     if (v & (MOE_DEVERR_EXPERT_RANGE | MOE_DEVERR_DUPLICATE)) return MOE_ERR_BAD_ROUTING;
     return MOE_OK;
 }

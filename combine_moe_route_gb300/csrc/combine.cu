@@ -49,7 +49,9 @@ __device__ __forceinline__ void fma_row(float (&acc)[8], float w, const uint4 v)
 
 // tok2row == nullptr reads row g*K + j (the layout a push-style return leaves
 // on the origin rank); rows = number of rows of y (indices outside are skipped).
-template <bool kOutF32>
+// kAfterWait: launched with programmatic stream serialization behind the
+// combine receive half's wait kernel; nothing is read before that grid is done.
+template <bool kOutF32, bool kAfterWait = false>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __nv_bfloat16 *__restrict__ y,
                                                                   const int32_t *__restrict__ tok2row,
                                                                   const float *__restrict__ topk_w, int T, int K,
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __nv_bfl
     __shared__ int32_t s_row[MOE_MAX_TOPK];
     __shared__ float s_w[MOE_MAX_TOPK];
     const int nchunk = H / 8;
+    if (kAfterWait) pdl_wait();
 
     for (long long g = blockIdx.x; g < T; g += gridDim.x) {
         __syncthreads();   // previous token's readers are done with s_row / s_w
@@ -114,6 +117,79 @@ cudaError_t launch_combine(const void *y, const int32_t *tok2row, const float *t
     else
         combine_kernel<false><<<(unsigned)grid, kCombineThreads, 0, stream>>>(yb, tok2row, topk_w, T, K, H, rows, out);
     return cudaGetLastError();
+}
+
+// --------------------------------------------------------------------------
+// split combine: send and receive halves
+// --------------------------------------------------------------------------
+// Perplexity, "Enabling trillion-parameter models on AWS EFA": combine, like
+// dispatch, is split into a sender half and a receiver half so the GPU can run
+// other work while transfers are pending ("MoE all-to-all over EFA"); the
+// receiver waits for completion and then accumulates the returned tokens into
+// the output ("Dispatch and combine"); within a node the buffers are mapped
+// into the peers, which push or pull tokens directly ("Send and receive
+// buffers").  Here every rank's expert outputs already sit in the one HBM, so
+// the send half publishes them: one release store per expert rank, ready[r] = 1.
+// The receive half waits (bounded) for every rank's flag, consumes it, and
+// pulls each token's K rows for the same fixed-order weighted sum as
+// moe_combine (the sum kernel is launched behind the wait with programmatic
+// stream serialization, so its blocks are resident when the wait ends).
+__global__ void combine_send_kernel(int32_t *ready, int R) {
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+#ifdef MOE_TEST_WITHHOLD_READY_RANK
+        // Test builds only: this rank never publishes, so the receive half's
+        // bounded wait runs out.
+        if (r == MOE_TEST_WITHHOLD_READY_RANK) continue;
+#endif
+        st_release_gpu(ready + r, 1);
+    }
+}
+
+__global__ void combine_wait_kernel(int32_t *ready, int R, int32_t *err) {
+    pdl_launch_dependents();   // the sum kernel may launch; it waits for this grid to finish
+    bool timed_out = false;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+        if (ld_acquire_gpu(ready + r) != 1) {
+            const uint64_t t0 = global_timer_ns();
+            while (!timed_out && ld_acquire_gpu(ready + r) != 1) {
+                if (global_timer_ns() - t0 > kWaitLimitNs) timed_out = true;
+                else __nanosleep(64);
+            }
+        }
+        ready[r] = 0;   // consumed: a second receive without a new send waits again
+    }
+    if (timed_out) set_device_error(err, MOE_DEVERR_RECV_TIMEOUT);
+}
+
+cudaError_t launch_combine_send(int R, void *workspace, cudaStream_t stream) {
+    int32_t *ready = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + kWsHeader) + R;
+    combine_send_kernel<<<1, 256, 0, stream>>>(ready, R);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_recv(const void *y, const int32_t *tok2row, const float *topk_w, int T, int K, int H,
+                                bool out_f32, void *out, int R, void *workspace, cudaStream_t stream) {
+    int32_t *err = static_cast<int32_t *>(workspace);
+    int32_t *ready = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + kWsHeader) + R;
+    combine_wait_kernel<<<1, 256, 0, stream>>>(ready, R, err);
+    cudaError_t ce = cudaGetLastError();
+    if (ce != cudaSuccess) return ce;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(T > 0 ? T : 1));   // one block per token, as moe_combine
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const __nv_bfloat16 *yb = static_cast<const __nv_bfloat16 *>(y);
+    const long long rows = (long long)T * K;
+    if (out_f32)
+        ce = cudaLaunchKernelEx(&cfg, combine_kernel<true, true>, yb, tok2row, topk_w, T, K, H, rows, out);
+    else
+        ce = cudaLaunchKernelEx(&cfg, combine_kernel<false, true>, yb, tok2row, topk_w, T, K, H, rows, out);
+    return ce;
 }
 
 // --------------------------------------------------------------------------

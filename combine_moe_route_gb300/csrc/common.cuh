@@ -149,6 +149,26 @@ __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned lon
 
 __device__ __forceinline__ void set_device_error(int32_t *err, int bits) { atomicOr(err, bits); }
 
+// Acquire load / release store and add of a 32-bit word in global memory, at
+// GPU scope (the split halves' signals).
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int32_t *p, int32_t v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_add_gpu(int32_t *p, int32_t v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Order this thread's completed async-proxy (bulk copy) writes to global
+// memory before its later generic-proxy operations.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Programmatic dependent launch: allow the next kernel in the stream (if it
 // was launched with programmatic stream serialization) to start now; wait
 // until the kernel this one depends on has finished and its writes are

@@ -75,20 +75,22 @@ namespace moe {
 // local_rank (aliases the tok2row output): in-tile rank of each item, or -1
 // (an expert id out of range; the scatter, which reads every id again,
 // reports it).  Block 0 also clears the call's workspace header (error word,
-// scan ticket, scatter token counter) and the lookback status words: nothing
-// reads or writes them before this grid has completed, so no memset has to
-// run ahead of this kernel.
+// scan ticket, scatter token counter), the split halves' signals and the
+// lookback status words: nothing reads or writes them before this grid has
+// completed, so no memset has to run ahead of this kernel.
 __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *__restrict__ topk_idx, int E, int K,
                                                                  const __grid_constant__ RankTable rt,
                                                                  int32_t *__restrict__ tile_hist,
                                                                  int32_t *__restrict__ local_rank,
                                                                  int32_t *__restrict__ header,
+                                                                 int32_t *__restrict__ signal, int nsignal,
                                                                  unsigned long long *__restrict__ status,
                                                                  int nstatus) {
     extern __shared__ int32_t hist[];   // [kHistWarps][E]
     pdl_launch_dependents();            // the scan may launch; it waits for this grid's writes
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i < (int)(kWsHeader / 4); i += blockDim.x) header[i] = 0;
+        for (int i = threadIdx.x; i < nsignal; i += blockDim.x) signal[i] = 0;
         for (int i = threadIdx.x; i < nstatus; i += blockDim.x) status[i] = 0ull;
     }
     const int tile = blockIdx.x;
@@ -296,6 +298,7 @@ struct ScatterArgs {
     int32_t *err;
     const int32_t *tile_hist;  // [E * ntiles] (low-latency layout)
     int32_t *next_token;       // token counter, zero at launch (workspace header)
+    int32_t *arrive;           // send half: copies landed per destination rank (zero at launch), else null
     int T, E, K, H;
     int C;                     // low-latency layout: rows per (expert, source rank) region
 };
@@ -315,7 +318,10 @@ __device__ __forceinline__ void quantize_block16(const uint4 xin, uint2 &qout, f
     for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    amax = fmaxf(amax, 0x1p-64f);
+    // raised to 2^-119, the smallest power of two with 448/amax finite in fp32:
+    // a zero or tiny block keeps finite scales, and its nonzero bf16 values
+    // (down to 2^-133) still map to nonzero codes
+    amax = fmaxf(amax, 0x1p-119f);
     scale_out = __fdiv_rn(amax, 448.0f);
     const float inv = __fdiv_rn(448.0f, amax);
     uint32_t w[4];
@@ -353,7 +359,10 @@ __device__ __forceinline__ void quantize_stage(unsigned char *buf, int H, int la
         const uint4 xin = valid ? src[b * 16 + hl] : make_uint4(0u, 0u, 0u, 0u);
         uint2 qo;
         float s;
-        quantize_block16(xin, qo, s);   // its shuffles order every lane's read before any write
+        quantize_block16(xin, qo, s);
+        // the second half-warp's codes land on bf16 bytes the first half-warp
+        // read in this step: every lane's read comes before any lane's write
+        __syncwarp();
         if (valid) {
             q[b * 16 + hl] = qo;
             if (hl == 0) sc[b] = s;
@@ -387,6 +396,12 @@ __device__ __forceinline__ void quantize_stage(unsigned char *buf, int H, int la
 // region by one atomic increment of the region's count (zeroed before the
 // launch), so neither histogram nor scan runs; the order of a region's rows is
 // whatever order the increments happened in.
+//
+// Send half of the split dispatch (a.arrive != null, ragged layout): the
+// counts / offsets / expert_offsets are left to the receive half, and every
+// warp tallies its copies per destination rank in shared memory; once its
+// last bulk stores have completed it adds the tallies to the per-rank arrival
+// counters with release semantics (the receive half waits for them).
 enum ScatterMode : int { kRagged = 0, kLowLatency = 1, kLowLatencyUnordered = 2 };
 
 template <bool kFp8, int kMode>
@@ -411,6 +426,16 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
 
     unsigned char *wbase = smem + (size_t)warp * S * stage_bytes;
     auto stage = [&](int it) { return wbase + (size_t)(it % S) * stage_bytes; };
+    // send half: this warp's copies per destination rank, after every warp's stages
+    const bool send = kMode == kRagged && a.arrive != nullptr;
+    const int L = E / rt.R;
+    int32_t *s_arr = send ? reinterpret_cast<int32_t *>(smem + (size_t)MOE_SCATTER_WARPS * S * stage_bytes) +
+                                (size_t)warp * rt.R
+                          : nullptr;
+    if (send) {
+        for (int r = lane; r < rt.R; r += 32) s_arr[r] = 0;
+        __syncwarp();
+    }
     // the first S tokens of warp w are w, w + W, ..., w + (S-1)W (W warps in
     // the grid), which spreads a small batch over every warp; the tokens from
     // S*W on are handed out by the counter
@@ -468,8 +493,9 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
             for (int tau = rt.tile_off[s]; tau < rt.tile_off[s + 1]; ++tau) c += a.tile_hist[(long long)e * rt.ntiles + tau];
             a.counts[i] = c;
         }
-    } else if (kMode == kRagged) {
-        // counts / offsets / expert_offsets from the scanned histogram
+    } else if (kMode == kRagged && !send) {
+        // counts / offsets / expert_offsets from the scanned histogram (the
+        // split dispatch writes them in its receive half)
         const int n = E * rt.R;
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= n; i += gridDim.x * blockDim.x) {
             if (i < n) {
@@ -492,6 +518,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
     for (int it = 0; failed_at < 0 && it < claimed; ++it) {
         const uint32_t parity = (uint32_t)((it / S) & 1);
         unsigned char *buf = stage(it);
+        int my_dest = -1;   // send half: destination rank of this lane's copy (lane j = copy j)
         // 1. destination rows (lane j = copy j)
         {
             const long long g = s_tok[warp][it % S];
@@ -536,6 +563,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
                 }
                 a.tok2row[i] = row;
                 s_rows[warp][lane] = row;
+                if (send && row >= 0) my_dest = e / L;
             }
             int dup = 0;
             for (int j = 0; j < K; ++j) {
@@ -552,6 +580,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
             failed_at = it;
             break;
         }
+        if (my_dest >= 0) atomicAdd(&s_arr[my_dest], 1);   // stored below
 
         // 3. quantise in place
         float *sc = reinterpret_cast<float *>(buf + (size_t)H * 2);
@@ -601,6 +630,319 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
                 (void)mbar_wait_bounded(&bars[warp][t % S], (uint32_t)((t / S) & 1));
         }
         bulk_wait_all();
+        if (send) {
+            // the bulk stores are complete; order them before the releases below
+            fence_proxy_async_global();
+            __threadfence();
+        }
+    }
+    if (send) {
+        __syncwarp();
+        for (int r = lane; r < rt.R; r += 32) {
+            const int c = s_arr[r];
+#ifdef MOE_TEST_WITHHOLD_ARRIVAL_RANK
+            // Test builds only: copies bound for this rank are never announced,
+            // so the receive half's bounded wait runs out.
+            if (r == MOE_TEST_WITHHOLD_ARRIVAL_RANK) continue;
+#endif
+            if (c > 0) red_release_add_gpu(a.arrive + r, c);
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// 4. small batches: count, scan and scatter in one kernel
+// --------------------------------------------------------------------------
+// Inside expert e's segment the rows follow the global (rank-major) token
+// order, so copy j of token g lands in
+//   row(g, j) = start(e) + #{tokens g' < g routed to e},  e = topk_idx[g, j],
+// where start(e) is the number of copies routed to the experts below e.  When
+// the batch has few items, every block can afford to count all of them and
+// the histogram and scan kernels (and the two kernel boundaries they cost)
+// drop out: block b takes the contiguous tokens [g0, g1), and
+//   A. each warp stages its first two source rows by bulk copy (they do not
+//      depend on the routing, so the loads overlap the counting);
+//   B. the block counts every item per expert (tot), the items before g0
+//      (pre), and, for the source rank s = b (then b + grid, ...), the items
+//      of the ranks below s (bef) and of rank s (ins);
+//   C. tot is scanned into start(e); the block writes rank s's layout --
+//      counts[e*R+s] = ins(e), offsets[e*R+s] = start(e) + bef(e) -- and ranks
+//      each of its own items among the earlier ones of its range;
+//   D. its warps scatter their tokens (one warp per token, two bulk-copy
+//      stages, in-place FP8) as the scatter kernel does.
+// The kernel runs behind a one-block kernel that clears the workspace header
+// and signals (programmatic stream serialization); it waits for that kernel
+// before it first touches either.  The send half of the split dispatch
+// (layout != null) writes offsets into the workspace, where its receive half
+// reads them, instead of the counts / offsets / expert_offsets outputs.
+constexpr int kSmallMaxWarps = 8;
+constexpr int kSmallStages = 2;
+#ifndef MOE_SMALL_DISPATCH_ITEMS
+#define MOE_SMALL_DISPATCH_ITEMS 32768   // T*K up to which a dispatch takes the one-kernel path
+#endif
+
+struct SmallArgs {
+    const __nv_bfloat16 *x;
+    const int32_t *topk_idx;
+    void *recv_x;
+    float *recv_scale;
+    int32_t *counts;           // null in the send half
+    int32_t *offsets;
+    int32_t *expert_offsets;
+    int32_t *layout;           // send half: offsets [E*R + 1] for the receive half, else null
+    int32_t *tok2row;
+    int32_t *row2src;
+    int32_t *err;
+    int32_t *arrive;           // send half: copies landed per destination rank, else null
+    int T, E, K, H;
+    int tpb;                   // tokens per block
+};
+
+// Bytes of dynamic shared memory of the one-kernel dispatch for W warps.
+__host__ __device__ inline size_t small_smem_bytes(int W, int H, bool fp8, int E, int R, int tpb, int K, bool send) {
+    size_t b = (size_t)W * kSmallStages * scatter_stage_bytes(H, fp8);
+    b += (size_t)4 * E * 4;                   // tot, pre, bef, ins
+    b += (size_t)2 * tpb * K * 4;             // the range's expert ids and rows
+    if (send) b += (size_t)W * R * 4;         // per-warp arrival tallies
+    return b;
+}
+
+__global__ void dispatch_prep_kernel(int32_t *__restrict__ header, int32_t *__restrict__ signal, int nsignal) {
+    pdl_launch_dependents();
+    for (int i = threadIdx.x; i < (int)(kWsHeader / 4); i += blockDim.x) header[i] = 0;
+    for (int i = threadIdx.x; i < nsignal; i += blockDim.x) signal[i] = 0;
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(const SmallArgs a,
+                                                                             const __grid_constant__ RankTable rt) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bars[kSmallMaxWarps][kSmallStages];
+    __shared__ int s_total;
+    constexpr int S = kSmallStages;
+    const int W = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int T = a.T, E = a.E, K = a.K, H = a.H, R = rt.R, L = E / R;
+    const int nblk = H / 128;
+    const size_t stage_bytes = scatter_stage_bytes(H, kFp8);
+    const uint32_t in_bytes = (uint32_t)H * 2u;
+    const uint32_t out_bytes = kFp8 ? (uint32_t)H : in_bytes;
+    const size_t recv_pitch = kFp8 ? (size_t)H : (size_t)H * 2;
+    const bool scale_bulk = kFp8 && (nblk * 4) % 16 == 0;
+    const bool send = a.arrive != nullptr;
+
+    const long long g0 = (long long)blockIdx.x * a.tpb;
+    const long long g1 = min(g0 + (long long)a.tpb, (long long)T);
+    const int ntok = (int)(g1 - g0);
+    const int my_n = ntok > warp ? (ntok - warp + W - 1) / W : 0;   // tokens g0 + warp + i*W
+
+    int32_t *tot = reinterpret_cast<int32_t *>(smem + (size_t)W * S * stage_bytes);
+    int32_t *pre = tot + E;
+    int32_t *bef = pre + E;
+    int32_t *ins = bef + E;
+    int32_t *s_idx = ins + E;                 // [tpb*K] expert ids of the block's items
+    int32_t *s_row = s_idx + a.tpb * K;       // [tpb*K] their rows
+    int32_t *s_arr = send ? s_row + a.tpb * K + warp * R : nullptr;
+    auto stage = [&](int it) { return smem + ((size_t)warp * S + (it % S)) * stage_bytes; };
+
+    // A. stage the first rows
+    if (lane == 0) {
+        for (int st = 0; st < S; ++st) mbar_init(&bars[warp][st], 1);
+        fence_proxy_async_smem();
+        for (int it = 0; it < S && it < my_n; ++it) {
+            const long long g = g0 + warp + (long long)it * W;
+            mbar_arrive_expect_tx(&bars[warp][it], in_bytes);
+            bulk_load(stage(it), a.x + g * H, in_bytes, &bars[warp][it]);
+        }
+    }
+
+    // B. counts
+    for (int i = threadIdx.x; i < 4 * E; i += blockDim.x) tot[i] = 0;
+    if (send)
+        for (int r = lane; r < R; r += 32) s_arr[r] = 0;
+    __syncthreads();
+    const long long n_all = (long long)T * K;
+    const long long pb = g0 * K;
+    auto count_pass = [&](long long lim, long long mlo, long long mhi, bool all) {
+        for (long long i = threadIdx.x; i < lim; i += blockDim.x) {
+            const int e = __ldg(a.topk_idx + i);
+            if ((unsigned)e >= (unsigned)E) continue;   // reported in D
+            if (all) {
+                atomicAdd(&tot[e], 1);
+                if (i < pb) atomicAdd(&pre[e], 1);
+            }
+            if (i < mlo)
+                atomicAdd(&bef[e], 1);
+            else if (i < mhi)
+                atomicAdd(&ins[e], 1);
+        }
+    };
+    int s_meta = blockIdx.x;
+    if (s_meta < R)
+        count_pass(n_all, (long long)rt.rank_off[s_meta] * K, (long long)rt.rank_off[s_meta + 1] * K, true);
+    else
+        count_pass(n_all, 0, 0, true);
+    for (int k = threadIdx.x; k < ntok * K; k += blockDim.x) s_idx[k] = __ldg(a.topk_idx + pb + k);
+    __syncthreads();
+
+    // C. start(e): exclusive scan of tot, in place (warp 0; E <= 1024)
+    if (warp == 0) {
+        const int per = (E + 31) >> 5;
+        int sum = 0;
+        for (int k = 0; k < per; ++k) {
+            const int e = lane * per + k;
+            if (e < E) sum += tot[e];
+        }
+        const int incl = warp_inclusive_scan(sum);
+        int run = incl - sum;
+        for (int k = 0; k < per; ++k) {
+            const int e = lane * per + k;
+            if (e < E) {
+                const int c = tot[e];
+                tot[e] = run;
+                run += c;
+            }
+        }
+        if (lane == 31) s_total = incl;
+    }
+    __syncthreads();
+    const int total = s_total;
+    // the layout of source ranks blockIdx.x, blockIdx.x + grid, ...
+    for (; s_meta < R; s_meta += gridDim.x) {
+        if (s_meta != (int)blockIdx.x) {   // a further rank: count again
+            __syncthreads();
+            for (int i = threadIdx.x; i < 2 * E; i += blockDim.x) bef[i] = 0;   // bef and ins
+            __syncthreads();
+            count_pass((long long)rt.rank_off[s_meta + 1] * K, (long long)rt.rank_off[s_meta] * K,
+                       (long long)rt.rank_off[s_meta + 1] * K, false);
+            __syncthreads();
+        }
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int o = tot[e] + bef[e];
+            if (a.layout) {
+                a.layout[e * R + s_meta] = o;
+            } else {
+                a.offsets[e * R + s_meta] = o;
+                a.counts[e * R + s_meta] = ins[e];
+                if (s_meta == 0) a.expert_offsets[e] = tot[e];
+            }
+        }
+        if (s_meta == R - 1 && threadIdx.x == 0) {
+            if (a.layout) {
+                a.layout[E * R] = total;
+            } else {
+                a.offsets[E * R] = total;
+                a.expert_offsets[E] = total;
+            }
+        }
+    }
+    // rows of the block's items: start + earlier tokens (before the range, then inside it)
+    for (int k = threadIdx.x; k < ntok * K; k += blockDim.x) {
+        const int e = s_idx[k];
+        int row = -1;
+        if ((unsigned)e < (unsigned)E) {
+            int rr = 0;
+            for (int k2 = 0; k2 < k; ++k2) rr += (s_idx[k2] == e) ? 1 : 0;
+            row = tot[e] + pre[e] + rr;
+        }
+        s_row[k] = row;
+    }
+    __syncthreads();
+
+    // D. scatter; the header (error word) and signals are cleared by the kernel ahead
+    pdl_wait();
+    int failed_at = -1;
+    for (int it = 0; failed_at < 0 && it < my_n; ++it) {
+        const uint32_t parity = (uint32_t)((it / S) & 1);
+        unsigned char *buf = stage(it);
+        const long long g = g0 + warp + (long long)it * W;
+        const int k0 = (int)(g - g0) * K;
+        int my_dest = -1;
+        {
+            int e = -1, row = -1;
+            if (lane < K) {
+                const long long i = g * K + lane;
+                e = s_idx[k0 + lane];
+                row = s_row[k0 + lane];
+                if ((unsigned)e >= (unsigned)E) {
+                    set_device_error(a.err, MOE_DEVERR_EXPERT_RANGE);
+                    e = -1;
+                    row = -1;
+                }
+                a.tok2row[i] = row;
+                if (row >= 0) {
+                    a.row2src[row] = (int32_t)i;
+                    if (send) my_dest = e / L;
+                }
+            }
+            int dup = 0;
+            for (int j = 0; j < K; ++j) {
+                const int ej = __shfl_sync(0xffffffffu, e, j);
+                if (lane < j && e >= 0 && e == ej) dup = 1;
+            }
+            if (__any_sync(0xffffffffu, dup) && lane == 0) set_device_error(a.err, MOE_DEVERR_DUPLICATE);
+        }
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][it % S], parity));
+        if (!ok) {
+            if (lane == 0) set_device_error(a.err, MOE_DEVERR_COPY_TIMEOUT);
+            failed_at = it;
+            break;
+        }
+        if (my_dest >= 0) atomicAdd(&s_arr[my_dest], 1);   // stored below
+        float *sc = reinterpret_cast<float *>(buf + (size_t)H * 2);
+        if (kFp8) quantize_stage(buf, H, lane);
+        __syncwarp();
+        if (lane == 0) {
+            for (int j = 0; j < K; ++j) {
+                const int row = s_row[k0 + j];
+                if (row < 0 || (unsigned)s_idx[k0 + j] >= (unsigned)E) continue;
+                bulk_store(static_cast<unsigned char *>(a.recv_x) + (size_t)row * recv_pitch, buf, out_bytes);
+                if (scale_bulk) bulk_store(a.recv_scale + (size_t)row * nblk, sc, (uint32_t)nblk * 4u);
+            }
+            bulk_commit();
+        }
+        if (kFp8 && !scale_bulk) {
+            for (int t = lane; t < K * nblk; t += 32) {
+                const int j = t / nblk;
+                const int b = t - j * nblk;
+                const int row = s_row[k0 + j];
+                if (row >= 0 && (unsigned)s_idx[k0 + j] < (unsigned)E) a.recv_scale[(size_t)row * nblk + b] = sc[b];
+            }
+        }
+        // refill the previous token's stage with token it - 1 + S once its stores have read it
+        if (lane == 0 && it >= 1 && it - 1 + S < my_n) {
+            bulk_wait_read<1>();
+            const int nxt = it - 1 + S;
+            const long long gn = g0 + warp + (long long)nxt * W;
+            mbar_arrive_expect_tx(&bars[warp][nxt % S], in_bytes);
+            bulk_load(stage(nxt), a.x + gn * H, in_bytes, &bars[warp][nxt % S]);
+        }
+        __syncwarp();
+    }
+    if (lane == 0) {
+        if (failed_at >= 0) {
+            // let every load this warp issued land before the block's shared memory goes away
+            // tokens whose loads were issued: the first S, then one per refill (iterations 1 .. failed_at-1)
+            const int issued = min(my_n, max(S, failed_at + S - 1));
+            for (int t = failed_at; t < issued; ++t)
+                (void)mbar_wait_bounded(&bars[warp][t % S], (uint32_t)((t / S) & 1));
+        }
+        bulk_wait_all();
+        if (send) {
+            fence_proxy_async_global();
+            __threadfence();
+        }
+    }
+    if (send) {
+        __syncwarp();
+        for (int r = lane; r < R; r += 32) {
+            const int c = s_arr[r];
+#ifdef MOE_TEST_WITHHOLD_ARRIVAL_RANK
+            if (r == MOE_TEST_WITHHOLD_ARRIVAL_RANK) continue;
+#endif
+            if (c > 0) red_release_add_gpu(a.arrive + r, c);
+        }
     }
 }
 
@@ -609,14 +951,17 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
 // --------------------------------------------------------------------------
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-// Workspace layout for a worst-case tile count.
-DispatchPlan plan_dispatch(int E, int ntiles) {
+size_t signal_workspace_bytes(int R) { return kWsHeader + align256((size_t)R * 2 * 4); }
+
+// Workspace layout for a tile count (a worst case, or the call's own).
+DispatchPlan plan_dispatch(int E, int R, int ntiles) {
     DispatchPlan p{};
     p.ntiles = ntiles;
     const long long n = (long long)E * ntiles;
     p.nscan_blocks = (int)((n + kScanChunk - 1) / kScanChunk);
     if (p.nscan_blocks < 1) p.nscan_blocks = 1;
-    p.off_status = kWsHeader;
+    p.off_signal = kWsHeader;   // arrive[R], then ready[R]
+    p.off_status = signal_workspace_bytes(R);
     p.off_hist = p.off_status + align256((size_t)p.nscan_blocks * 8);
     p.off_scan = p.off_hist + align256((size_t)n * 4);
     p.total = p.off_scan + align256((size_t)(n + 1) * 4);
@@ -647,9 +992,9 @@ int device_sm_count() { return sm_count(); }
 // current device.  The kernel's shared-memory limit is only ever raised and the
 // occupancy is asked once per (kernel, device, size): both are host calls that
 // would otherwise sit on every launch's critical path.
-static cudaError_t scatter_blocks_per_sm(const void *kfn, size_t smem, int *per_sm) {
+static cudaError_t kernel_blocks_per_sm(const void *kfn, int threads, size_t smem, int *per_sm) {
     struct Limit { const void *fn; int dev; size_t smem; };
-    struct Occ { const void *fn; int dev; size_t smem; int per_sm; };
+    struct Occ { const void *fn; int dev; int threads; size_t smem; int per_sm; };
     static std::mutex mu;
     static Limit limits[16];
     static int nlimits = 0;
@@ -660,7 +1005,7 @@ static cudaError_t scatter_blocks_per_sm(const void *kfn, size_t smem, int *per_
     if (ce != cudaSuccess) return ce;
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < noccs; ++i)
-        if (occs[i].fn == kfn && occs[i].dev == dev && occs[i].smem == smem) {
+        if (occs[i].fn == kfn && occs[i].dev == dev && occs[i].threads == threads && occs[i].smem == smem) {
             *per_sm = occs[i].per_sm;
             return cudaSuccess;
         }
@@ -676,9 +1021,8 @@ static cudaError_t scatter_blocks_per_sm(const void *kfn, size_t smem, int *per_
             limits[nlimits++] = Limit{kfn, dev, smem};
     }
     int n = 0;
-    if ((ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kfn, MOE_SCATTER_WARPS * 32, smem)) != cudaSuccess)
-        return ce;
-    if (noccs < 64) occs[noccs++] = Occ{kfn, dev, smem, n};
+    if ((ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kfn, threads, smem)) != cudaSuccess) return ce;
+    if (noccs < 64) occs[noccs++] = Occ{kfn, dev, threads, smem, n};
     *per_sm = n;
     return cudaSuccess;
 }
@@ -690,19 +1034,24 @@ static const void *scatter_fn(bool fp8) {
     return fp8 ? (const void *)scatter_kernel<true, kMode> : (const void *)scatter_kernel<false, kMode>;
 }
 
-static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, int mode, cudaStream_t stream) {
+// max_sms > 0 caps the SMs the persistent grid spans (work on other streams
+// can then run on the rest); the build-time MOE_SCATTER_MAX_SMS caps it too.
+static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, int mode, cudaStream_t stream,
+                                  int max_sms = 0) {
     const long long T = a.T;
     const int H = a.H;
     cudaError_t ce;
-    const size_t smem = scatter_stage_bytes(H, fp8) * MOE_SCATTER_STAGES * MOE_SCATTER_WARPS;
+    const size_t arrive_smem = a.arrive ? (size_t)rt.R * 4 * MOE_SCATTER_WARPS : 0;   // send half's tallies
+    const size_t smem = scatter_stage_bytes(H, fp8) * MOE_SCATTER_STAGES * MOE_SCATTER_WARPS + arrive_smem;
     const void *kfn = mode == kRagged       ? scatter_fn<kRagged>(fp8)
                       : mode == kLowLatency ? scatter_fn<kLowLatency>(fp8)
                                             : scatter_fn<kLowLatencyUnordered>(fp8);
     int per_sm = 0;
-    if ((ce = scatter_blocks_per_sm(kfn, smem, &per_sm)) != cudaSuccess) return ce;
+    if ((ce = kernel_blocks_per_sm(kfn, MOE_SCATTER_WARPS * 32, smem, &per_sm)) != cudaSuccess) return ce;
     if (per_sm < 1) per_sm = 1;
     int sms = sm_count();
     if (MOE_SCATTER_MAX_SMS > 0 && MOE_SCATTER_MAX_SMS < sms) sms = MOE_SCATTER_MAX_SMS;
+    if (max_sms > 0 && max_sms < sms) sms = max_sms;
     long long grid = (long long)sms * per_sm;   // persistent: one wave
     const long long need = (T + MOE_SCATTER_WARPS - 1) / MOE_SCATTER_WARPS;
     if (grid > need) grid = need;
@@ -724,15 +1073,103 @@ static cudaError_t launch_scatter(ScatterArgs a, const RankTable &rt, bool fp8, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
-                            bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *offsets,
-                            int32_t *expert_offsets, int32_t *tok2row, int32_t *row2src, void *workspace,
-                            cudaStream_t stream) {
+bool small_dispatch(long long T, int K) { return T > 0 && T * K <= (long long)MOE_SMALL_DISPATCH_ITEMS; }
+
+// The workspace layout of a call: the one-kernel path keeps one scan entry
+// per (expert, source rank) (the send half leaves the offsets there for the
+// receive half), the three-kernel path one per (expert, tile).
+DispatchPlan call_plan(const RankTable &rt, int E, int K) {
+    return plan_dispatch(E, rt.R, small_dispatch(rt.rank_off[rt.R], K) ? rt.R : rt.ntiles);
+}
+
+// prep (clears the header and signals) + the one-kernel dispatch
+static cudaError_t launch_dispatch_small(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K,
+                                         int H, bool fp8, void *recv_x, float *recv_scale, int32_t *counts,
+                                         int32_t *offsets, int32_t *expert_offsets, int32_t *tok2row,
+                                         int32_t *row2src, void *workspace, bool send, int max_sms,
+                                         cudaStream_t stream) {
     const long long T = rt.rank_off[rt.R];
-    const DispatchPlan p = plan_dispatch(E, rt.ntiles);
+    const DispatchPlan p = call_plan(rt, E, K);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    int32_t *signal = reinterpret_cast<int32_t *>(ws + p.off_signal);
+    int sms = sm_count();
+    if (max_sms > 0 && max_sms < sms) sms = max_sms;
+    // warps per block: as many (up to 8) as two stages of rows per warp leave room for
+    const size_t smem_cap = 227 * 1024 - 1024;
+    int W = 0, tpb = 0;
+    long long grid = 0;
+    size_t smem = 0;
+    for (int w = kSmallMaxWarps; w >= 1 && W == 0; --w) {
+        long long gr = (T + w - 1) / w;
+        if (gr > sms) gr = sms;
+        const int tp = (int)((T + gr - 1) / gr);
+        gr = (T + tp - 1) / tp;   // every block has at least one token
+        const size_t sm = small_smem_bytes(w, H, fp8, E, rt.R, tp, K, send);
+        if (sm <= smem_cap) {
+            W = w;
+            tpb = tp;
+            grid = gr;
+            smem = sm;
+        }
+    }
+    if (W == 0) return cudaErrorInvalidConfiguration;   // unreachable for H <= MOE_MAX_HIDDEN
+    const void *kfn = fp8 ? (const void *)dispatch_small_kernel<true> : (const void *)dispatch_small_kernel<false>;
+    int per_sm = 0;
+    cudaError_t ce;
+    if ((ce = kernel_blocks_per_sm(kfn, W * 32, smem, &per_sm)) != cudaSuccess) return ce;
+
+    dispatch_prep_kernel<<<1, 256, 0, stream>>>(reinterpret_cast<int32_t *>(ws), signal, 2 * rt.R);
+    if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
+
+    SmallArgs a{};
+    a.x = static_cast<const __nv_bfloat16 *>(x);
+    a.topk_idx = topk_idx;
+    a.recv_x = recv_x;
+    a.recv_scale = recv_scale;
+    a.counts = counts;
+    a.offsets = offsets;
+    a.expert_offsets = expert_offsets;
+    a.layout = send ? reinterpret_cast<int32_t *>(ws + p.off_scan) : nullptr;
+    a.tok2row = tok2row;
+    a.row2src = row2src;
+    a.err = reinterpret_cast<int32_t *>(ws);
+    a.arrive = send ? signal : nullptr;
+    a.T = (int)T;
+    a.E = E;
+    a.K = K;
+    a.H = H;
+    a.tpb = tpb;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(W * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *params[] = {&a, const_cast<RankTable *>(&rt)};
+    if ((ce = cudaLaunchKernelExC(&cfg, kfn, params)) != cudaSuccess) return ce;
+    return cudaGetLastError();
+}
+
+// hist + scan + scatter; send: the split dispatch's send half (arrival
+// counters instead of counts / offsets / expert_offsets).
+static cudaError_t launch_dispatch_impl(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K,
+                                        int H, bool fp8, void *recv_x, float *recv_scale, int32_t *counts,
+                                        int32_t *offsets, int32_t *expert_offsets, int32_t *tok2row,
+                                        int32_t *row2src, void *workspace, bool send, int max_sms,
+                                        cudaStream_t stream) {
+    const long long T = rt.rank_off[rt.R];
+    if (small_dispatch(T, K))
+        return launch_dispatch_small(x, topk_idx, rt, E, K, H, fp8, recv_x, recv_scale, counts, offsets,
+                                     expert_offsets, tok2row, row2src, workspace, send, max_sms, stream);
+    const DispatchPlan p = plan_dispatch(E, rt.R, rt.ntiles);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     int32_t *err = reinterpret_cast<int32_t *>(ws);
     int32_t *ticket = reinterpret_cast<int32_t *>(ws + 4);   // scan block start order
+    int32_t *signal = reinterpret_cast<int32_t *>(ws + p.off_signal);
     unsigned long long *status = reinterpret_cast<unsigned long long *>(ws + p.off_status);
     int32_t *tile_hist = reinterpret_cast<int32_t *>(ws + p.off_hist);
     int32_t *scan = reinterpret_cast<int32_t *>(ws + p.off_scan);
@@ -740,7 +1177,7 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
     cudaError_t ce;
     const size_t hist_smem = (size_t)kHistWarps * E * 4;
     tile_hist_kernel<<<rt.ntiles, kHistThreads, hist_smem, stream>>>(topk_idx, E, K, rt, tile_hist, tok2row, err,
-                                                                     status, p.nscan_blocks);
+                                                                     signal, 2 * rt.R, status, p.nscan_blocks);
     if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
 
     const int n = E * rt.ntiles;
@@ -772,18 +1209,102 @@ cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTa
     a.row2src = row2src;
     a.err = err;
     a.next_token = reinterpret_cast<int32_t *>(ws + 8);   // scatter token counter
+    a.arrive = send ? signal : nullptr;
     a.T = (int)T;
     a.E = E;
     a.K = K;
     a.H = H;
-    return launch_scatter(a, rt, fp8, kRagged, stream);
+    return launch_scatter(a, rt, fp8, kRagged, stream, max_sms);
+}
+
+cudaError_t launch_dispatch(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
+                            bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *offsets,
+                            int32_t *expert_offsets, int32_t *tok2row, int32_t *row2src, void *workspace,
+                            cudaStream_t stream) {
+    return launch_dispatch_impl(x, topk_idx, rt, E, K, H, fp8, recv_x, recv_scale, counts, offsets, expert_offsets,
+                                tok2row, row2src, workspace, false, 0, stream);
+}
+
+cudaError_t launch_dispatch_send(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
+                                 bool fp8, void *recv_x, float *recv_scale, int32_t *tok2row, int32_t *row2src,
+                                 void *workspace, int max_sms, cudaStream_t stream) {
+    return launch_dispatch_impl(x, topk_idx, rt, E, K, H, fp8, recv_x, recv_scale, nullptr, nullptr, nullptr,
+                                tok2row, row2src, workspace, true, max_sms, stream);
+}
+
+// --------------------------------------------------------------------------
+// receive half of the split dispatch
+// --------------------------------------------------------------------------
+// Perplexity, "Enabling trillion-parameter models on AWS EFA", "Dispatch and
+// combine": the receiver blocks until every transfer to it has landed, then
+// hands the rows to the grouped GEMM.  Block r is destination rank r: thread 0
+// waits (bounded) until the copies announced for rank r equal the rows its
+// experts own in the scanned layout, consumes the counter (so a second
+// receive without a new send waits again), and the block writes the
+// receiver-side layout of rank r's experts: counts, offsets, expert_offsets.
+// A wait is skipped when the routing was already reported bad (the copies
+// never placed are then not awaited).
+__global__ void __launch_bounds__(256) dispatch_recv_kernel(const int32_t *__restrict__ scan,
+                                                            const __grid_constant__ RankTable rt, int E,
+                                                            int32_t *arrive, int32_t *err, int32_t *__restrict__ counts,
+                                                            int32_t *__restrict__ offsets,
+                                                            int32_t *__restrict__ expert_offsets) {
+    const int r = blockIdx.x;
+    const int R = rt.R;
+    const int L = E / R;
+    const long long nt = rt.ntiles;
+    if (threadIdx.x == 0) {
+        const int expected = scan[(long long)(r + 1) * L * nt] - scan[(long long)r * L * nt];
+        if (ld_acquire_gpu(arrive + r) != expected) {
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_gpu(arrive + r) != expected) {
+                if (ld_acquire_gpu(err) & (MOE_DEVERR_EXPERT_RANGE | MOE_DEVERR_DUPLICATE)) break;
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    set_device_error(err, MOE_DEVERR_RECV_TIMEOUT);
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        arrive[r] = 0;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < L * R; i += blockDim.x) {
+        const int e = r * L + i / R;
+        const int s = i - (i / R) * R;
+        const int o = scan[(long long)e * nt + rt.tile_off[s]];
+        const int o1 = scan[(long long)e * nt + rt.tile_off[s + 1]];
+        offsets[e * R + s] = o;
+        counts[e * R + s] = o1 - o;
+        if (s == 0) expert_offsets[e] = o;
+    }
+    if (r == R - 1 && threadIdx.x == 0) {
+        const int total = scan[(long long)E * nt];
+        offsets[E * R] = total;
+        expert_offsets[E] = total;
+    }
+}
+
+cudaError_t launch_dispatch_recv(const RankTable &rt_in, int E, int K, int32_t *counts, int32_t *offsets,
+                                 int32_t *expert_offsets, void *workspace, cudaStream_t stream) {
+    const DispatchPlan p = call_plan(rt_in, E, K);
+    RankTable rt = rt_in;
+    if (small_dispatch(rt.rank_off[rt.R], K)) {   // the send half left offsets[e*R + s]: one "tile" per rank
+        rt.ntiles = rt.R;
+        for (int s = 0; s <= rt.R; ++s) rt.tile_off[s] = s;
+    }
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    dispatch_recv_kernel<<<rt.R, 256, 0, stream>>>(reinterpret_cast<const int32_t *>(ws + p.off_scan), rt, E,
+                                                   reinterpret_cast<int32_t *>(ws + p.off_signal),
+                                                   reinterpret_cast<int32_t *>(ws), counts, offsets, expert_offsets);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch_ll(const void *x, const int32_t *topk_idx, const RankTable &rt, int E, int K, int H,
                                int C, bool fp8, void *recv_x, float *recv_scale, int32_t *counts, int32_t *tok2row,
                                int32_t *row2src, void *workspace, cudaStream_t stream) {
     const long long T = rt.rank_off[rt.R];
-    const DispatchPlan p = plan_dispatch(E, rt.ntiles);
+    const DispatchPlan p = plan_dispatch(E, rt.R, rt.ntiles);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     int32_t *err = reinterpret_cast<int32_t *>(ws);
     int32_t *tile_hist = reinterpret_cast<int32_t *>(ws + p.off_hist);
@@ -791,7 +1312,7 @@ cudaError_t launch_dispatch_ll(const void *x, const int32_t *topk_idx, const Ran
     cudaError_t ce;
     const size_t hist_smem = (size_t)kHistWarps * E * 4;
     tile_hist_kernel<<<rt.ntiles, kHistThreads, hist_smem, stream>>>(topk_idx, E, K, rt, tile_hist, tok2row, err,
-                                                                     nullptr, 0);
+                                                                     nullptr, 0, nullptr, 0);
     if ((ce = cudaGetLastError()) != cudaSuccess) return ce;
 
     ScatterArgs a{};

@@ -27,6 +27,7 @@
 
 #include <mutex>
 
+#include "launch.h"
 #include "moe_route.h"
 
 namespace {
@@ -58,22 +59,20 @@ extern "C" MOE_API moe_status moe_dispatch_noalloc(const void *x, const int32_t 
                                                    float *recv_scale, int32_t *counts, int32_t *offsets,
                                                    int32_t *expert_offsets, int32_t *tok2row, int32_t *row2src,
                                                    moe_stream_t stream) {
-    // Sizes first, on the host: an argument moe_dispatch would reject is passed
-    // through unchanged so that it reports the same status.
-    if (B == nullptr || R < 1 || R > MOE_MAX_RANKS)
+    // moe_dispatch's own argument checks come first, so a call it would reject
+    // reports the same status here; only a call that is otherwise valid can be
+    // refused for its size.
+    moe::RankTable rt;
+    long long T = 0;
+    bool fp8 = false;
+    const moe_status v = moe::check_dispatch_args(x, topk_idx, R, B, E, K, H, recv_dtype, recv_x, recv_scale, true,
+                                                  counts, offsets, expert_offsets, tok2row, row2src, rt, T, fp8);
+    if (v != MOE_OK) return v;
+    if (T == 0)   // nothing to scatter: moe_dispatch zero-fills the layout without a workspace
         return moe_dispatch(x, topk_idx, R, B, E, K, H, recv_dtype, recv_x, recv_scale, counts, offsets,
                             expert_offsets, tok2row, row2src, nullptr, 0, stream);
-    int64_t T = 0;
-    bool negative = false;
-    for (int s = 0; s < R; ++s) {
-        negative = negative || B[s] < 0;
-        T += B[s];
-    }
-    const size_t need = negative ? 0 : moe_dispatch_workspace_bytes(R, E, K, T);
-    if (need == 0 || T == 0)   // invalid sizes, or nothing to scatter: no workspace involved
-        return moe_dispatch(x, topk_idx, R, B, E, K, H, recv_dtype, recv_x, recv_scale, counts, offsets,
-                            expert_offsets, tok2row, row2src, nullptr, 0, stream);
-    if (need > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;   // beyond the static maximum
+    if (moe_dispatch_workspace_bytes(R, E, K, T) > (size_t)MOE_NOALLOC_SCRATCH_BYTES)
+        return MOE_ERR_WORKSPACE;   // beyond the static maximum
 
     void *scratch = nullptr;
     const moe_status st = scratch_address(&scratch);

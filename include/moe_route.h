@@ -91,6 +91,7 @@ typedef enum {
 #define MOE_DEVERR_DUPLICATE 0x2      /* the same expert twice in one token's top-K */
 #define MOE_DEVERR_SCAN_TIMEOUT 0x4   /* the decoupled-lookback wait ran out */
 #define MOE_DEVERR_COPY_TIMEOUT 0x8   /* a bulk-copy barrier wait ran out */
+#define MOE_DEVERR_RECV_TIMEOUT 0x10  /* a receive half's wait for its send half ran out */
 
 /* Returns MOE_ROUTE_ABI_VERSION of the loaded library. */
 MOE_API int moe_abi_version(void);
@@ -164,8 +165,10 @@ MOE_API size_t moe_dispatch_workspace_bytes(int R, int E, int K, int64_t T);
  *   H          hidden size, 8..MOE_MAX_HIDDEN, a multiple of 8; a multiple of
  *              128 when recv_dtype is MOE_DTYPE_FP8_E4M3.
  *   recv_dtype MOE_DTYPE_BF16 (copy) or MOE_DTYPE_FP8_E4M3 (quantise once per
- *              token: per 128-channel block, amax = max |x| floored at 2^-64,
- *              scale = amax / 448 and inv = 448 / amax (IEEE fp32 divisions),
+ *              token: per 128-channel block, amax = max |x| raised to at
+ *              least 2^-119 (the smallest power of two with 448 / amax finite
+ *              in fp32), scale = amax / 448 and inv = 448 / amax (IEEE fp32
+ *              divisions, subnormal results kept),
  *              q = e4m3(x * inv) with round-to-nearest-even and saturation to
  *              +-448; [DSD] "Quantization").
  *   recv_x     device [T*K, H] of recv_dtype, 16-byte aligned: out.  Rows are
@@ -219,8 +222,11 @@ MOE_API moe_status moe_dispatch(const void *x, const int32_t *topk_idx,
  *     call on each device before any stream capture.
  *   - Size limit: a call for which moe_dispatch_workspace_bytes(R, E, K, T)
  *     exceeds MOE_NOALLOC_SCRATCH_BYTES returns MOE_ERR_WORKSPACE and enqueues
- *     nothing (1 MiB covers, for example, E = 256 experts with T*K up to
- *     about 880 000 routed copies).
+ *     nothing; it does so only once moe_dispatch's own argument checks have
+ *     passed (a call those reject gets moe_dispatch's status).  The limit
+ *     depends on R, E and K: with E = 256 experts it is
+ *     T*K <= (511 - R) * 2048 routed copies (1 030 144 at R = 8, 784 384 at
+ *     R = 128); with E = 384 and R = 32 it is T*K <= 632 832.
  *   - Sharing: every call on a device uses the same array, which keeps the
  *     last call's contents; each call clears the parts that must start at
  *     zero.  Calls that overlap on the GPU (other streams, other threads)
@@ -394,6 +400,79 @@ MOE_API moe_status moe_combine_partial_send(const void *y, const int32_t *tok2ro
 MOE_API moe_status moe_combine_partial_recv(const void *partial, const int32_t *topk_idx, int T, int K, int H,
                                             int E, int R, moe_dtype out_dtype, void *out,
                                             moe_stream_t stream);
+
+/*
+ * Split dispatch and combine: each is cut into a send half and a receive half
+ * ([EFA] "MoE all-to-all over EFA": so that the GPU can run other work, such
+ * as the shared expert, while transfers are pending; the receiver blocks until
+ * every transfer to it has landed.  [DSD] "Computation and communication
+ * overlap": the shared expert runs right after Dispatch Send, and Dispatch
+ * Recv is awaited after it).  Results equal moe_dispatch's and moe_combine's
+ * bit for bit.
+ *
+ * Ordering: enqueue each receive half after its send half -- on the same
+ * stream, or on another stream behind an event recorded after the send half.
+ * The receive half's wait then confirms, per destination rank, that every
+ * transfer the send half announced has landed; it never waits on a kernel
+ * that is still to run.  If an announcement never comes the wait gives up
+ * after about 2 s, sets MOE_DEVERR_RECV_TIMEOUT in the workspace's error word
+ * (moe_get_device_error then returns MOE_ERR_TIMEOUT) and the call completes.
+ * The four calls of a layer share one workspace of at least
+ * moe_dispatch_workspace_bytes(R, E, K, T) bytes, 16-byte aligned; calls that
+ * share a workspace must not overlap in time apart from this pairing.
+ *
+ * moe_dispatch_send -- the copies ([EFA] "Dispatch and combine": per-expert
+ * counts by shared-memory atomics, a prefix sum for the offsets, tokens packed
+ * for their peers; within a node pushed straight into the peers' buffers).
+ * Histogram, scan and scatter of moe_dispatch: recv_x, recv_scale, tok2row
+ * and row2src are written exactly as moe_dispatch writes them; every copy is
+ * announced to its destination rank once its bytes are stored.  counts,
+ * offsets and expert_offsets are the receive half's.
+ *   arguments  as moe_dispatch, without counts, offsets and expert_offsets;
+ *   max_sms    0: the copy kernel may span every SM; n > 0: at most n SMs, so
+ *              that work the caller runs on another stream meanwhile keeps
+ *              the others.
+ * Errors: as moe_dispatch; MOE_ERR_INVALID_ARG for max_sms < 0.  T == 0
+ * launches nothing.
+ *
+ * moe_dispatch_recv -- the receiver's wait ([EFA] "Dispatch and combine":
+ * block until all transfers have landed, then hand the rows to the grouped
+ * GEMM): per destination rank r, waits until the copies announced for r equal
+ * the rows its experts own, consumes the announcements (a second receive
+ * without a new send waits again), and writes counts, offsets and
+ * expert_offsets as moe_dispatch defines them.  R, B, E, K and workspace are
+ * the send half's.  Errors: MOE_ERR_INVALID_ARG / MOE_ERR_WORKSPACE /
+ * MOE_ERR_UNSUPPORTED / MOE_ERR_CUDA.  T == 0 writes zeros and launches no
+ * kernel.
+ *
+ * moe_combine_send -- the expert ranks publish their outputs: one release
+ * flag per expert rank, set after the work enqueued before this call on
+ * `stream` (the expert GEMM that wrote y).  Every rank's buffer is in the one
+ * HBM, so the receive half pulls the rows itself ([EFA] "Send and receive
+ * buffers": within a node the buffers are mapped into the peers, which push
+ * or pull tokens directly) and nothing is copied here.
+ *   workspace  at least 256 + 8*R bytes rounded up to a multiple of 256 (the
+ *              layer's dispatch workspace is larger).
+ * Errors: MOE_ERR_INVALID_ARG for R out of range, MOE_ERR_WORKSPACE,
+ * MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA.
+ *
+ * moe_combine_recv -- waits until every expert rank's flag is set, consumes
+ * the flags, then forms out[g] exactly as moe_combine does ([EFA] "Dispatch
+ * and combine": the receiver accumulates the returned tokens into the output).
+ * Arguments as moe_combine, plus R and the workspace of moe_combine_send.
+ * Errors: as moe_combine; MOE_ERR_WORKSPACE.  T == 0 launches nothing.
+ */
+MOE_API moe_status moe_dispatch_send(const void *x, const int32_t *topk_idx, int R, const int32_t *B, int E, int K,
+                                     int H, moe_dtype recv_dtype, void *recv_x, float *recv_scale, int32_t *tok2row,
+                                     int32_t *row2src, int max_sms, void *workspace, size_t workspace_bytes,
+                                     moe_stream_t stream);
+MOE_API moe_status moe_dispatch_recv(int R, const int32_t *B, int E, int K, int32_t *counts, int32_t *offsets,
+                                     int32_t *expert_offsets, void *workspace, size_t workspace_bytes,
+                                     moe_stream_t stream);
+MOE_API moe_status moe_combine_send(int R, void *workspace, size_t workspace_bytes, moe_stream_t stream);
+MOE_API moe_status moe_combine_recv(const void *y, const int32_t *tok2row, const float *topk_w, int T, int K, int H,
+                                    moe_dtype out_dtype, void *out, int R, void *workspace, size_t workspace_bytes,
+                                    moe_stream_t stream);
 
 /*
  * moe_get_device_error -- SYNCHRONOUS: waits for `stream`, then copies the

@@ -286,3 +286,82 @@ def test_plain_c_consumer_compiles_and_links(lib, tmp_path):
     from combine_moe_route_gb300 import build
     exe = _c_abi.compile_roundtrip(build.library_path(), str(tmp_path))
     assert os.path.exists(exe)
+
+
+def test_split_halves_validation(lib):
+    """moe_dispatch_send / _recv and moe_combine_send / _recv reject bad arguments on the host.
+    (T == 0 is left out of the receive half: it zeroes counts, here a fake pointer.)"""
+    B = _B(3, 0, 5, 1)
+
+    def send(B, E=16, K=2, H=256, dtype=BF16, x=FAKE, recv=FAKE, scale=FAKE, max_sms=0, ws=FAKE, ws_bytes=1 << 30):
+        return lib.moe_dispatch_send(x, FAKE, B.size, B.ctypes.data, E, K, H, dtype, recv, scale, FAKE, FAKE,
+                                     max_sms, ws, ws_bytes, None)
+
+    assert send(_B()) == INVALID                                        # R = 0
+    assert send(B, E=18) == INVALID                                     # E % R
+    assert send(B, K=17) == INVALID                                     # K > E
+    assert send(B, H=264, dtype=FP8) == INVALID                         # FP8 needs H % 128
+    assert send(_B(3, -1, 5, 1)) == INVALID                             # negative B
+    assert send(B, x=None) == INVALID
+    assert send(B, max_sms=-1) == INVALID
+    assert send(B, ws=None) == WORKSPACE
+    assert send(B, ws_bytes=256) == WORKSPACE                           # header only
+    assert send(B, x=FAKE_MISALIGNED) == UNSUPPORTED
+    assert send(B, ws=FAKE_MISALIGNED) == UNSUPPORTED
+    assert send(_B(0, 0, 0, 0), x=None, recv=None) == OK                # T = 0: nothing to send
+
+    def recv(B, E=16, K=2, counts=FAKE, ws=FAKE, ws_bytes=1 << 30):
+        return lib.moe_dispatch_recv(B.size, B.ctypes.data, E, K, counts, FAKE, FAKE, ws, ws_bytes, None)
+
+    assert recv(_B()) == INVALID
+    assert recv(B, E=18) == INVALID
+    assert recv(B, K=0) == INVALID
+    assert recv(_B(3, -1, 5, 1)) == INVALID
+    assert recv(B, counts=None) == INVALID
+    assert recv(B, ws=None) == WORKSPACE
+    assert recv(B, ws_bytes=256) == WORKSPACE                           # header only
+    assert recv(B, ws=FAKE_MISALIGNED) == UNSUPPORTED
+
+    cs = lib.moe_combine_send               # (R, ws, ws_bytes, stream)
+    assert cs(0, FAKE, 1 << 20, None) == INVALID
+    assert cs(257, FAKE, 1 << 20, None) == INVALID
+    assert cs(4, None, 1 << 20, None) == WORKSPACE
+    assert cs(4, FAKE, 256, None) == WORKSPACE                          # header only, no flags
+    assert cs(4, FAKE_MISALIGNED, 1 << 20, None) == UNSUPPORTED
+    cr = lib.moe_combine_recv               # (y, tok2row, w, T, K, H, out_dtype, out, R, ws, ws_bytes, stream)
+    assert cr(FAKE, FAKE, FAKE, -1, 2, 256, BF16, FAKE, 4, FAKE, 1 << 20, None) == INVALID
+    assert cr(FAKE, FAKE, FAKE, 4, 33, 256, BF16, FAKE, 4, FAKE, 1 << 20, None) == INVALID
+    assert cr(FAKE, FAKE, FAKE, 4, 2, 250, BF16, FAKE, 4, FAKE, 1 << 20, None) == INVALID
+    assert cr(FAKE, FAKE, FAKE, 4, 2, 256, FP8, FAKE, 4, FAKE, 1 << 20, None) == INVALID
+    assert cr(FAKE, FAKE, FAKE, 4, 2, 256, BF16, FAKE, 0, FAKE, 1 << 20, None) == INVALID
+    assert cr(FAKE, None, FAKE, 4, 2, 256, BF16, FAKE, 4, FAKE, 1 << 20, None) == INVALID
+    assert cr(FAKE_MISALIGNED, FAKE, FAKE, 4, 2, 256, BF16, FAKE, 4, FAKE, 1 << 20, None) == UNSUPPORTED
+    assert cr(FAKE, FAKE, FAKE, 4, 2, 256, BF16, FAKE, 4, None, 1 << 20, None) == WORKSPACE
+    assert cr(FAKE, FAKE, FAKE, 4, 2, 256, BF16, FAKE, 4, FAKE, 256, None) == WORKSPACE
+    assert cr(None, None, None, 0, 2, 256, BF16, None, 4, None, 0, None) == OK
+
+
+def test_dispatch_noalloc_reports_argument_errors_before_its_size_limit(lib):
+    """A call moe_dispatch rejects for its arguments gets moe_dispatch's status, even when its
+    sizes are also beyond the static scratch; only an otherwise valid call gets
+    MOE_ERR_WORKSPACE."""
+    import ctypes
+    f = lib.moe_dispatch_noalloc
+    vp, i32 = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    f.restype = i32
+    big = _B(8192)                          # E = 1024, K = 32: beyond the scratch
+
+    def call(H=256, dtype=BF16, x=FAKE, recv=FAKE, scale=FAKE, counts=FAKE):
+        return f(x, FAKE, 1, big.ctypes.data, 1024, 32, H, dtype, recv, scale, counts, FAKE, FAKE, FAKE, FAKE, None)
+
+    assert call() == WORKSPACE
+    assert call(H=12) == INVALID                                        # H % 8
+    assert call(H=264, dtype=FP8) == INVALID                            # FP8 needs H % 128
+    assert call(dtype=FP32) == INVALID
+    assert call(x=None) == INVALID
+    assert call(counts=None) == INVALID
+    assert call(dtype=FP8, scale=None) == INVALID
+    assert call(x=FAKE_MISALIGNED) == UNSUPPORTED
+    assert call(recv=FAKE_MISALIGNED) == UNSUPPORTED
+    assert call(dtype=FP8, scale=FAKE_MISALIGNED) == UNSUPPORTED

@@ -343,11 +343,15 @@ def test_cuda_graph_replay_matches_eager(gpu):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("amax", [448.0, 224.0, 3.0625, 1.0, 0.7734375, 2.0**-10, 0.0311279296875, 5.5625,
-                                  17.875, 123.0, 300.0, 447.0])
+                                  17.875, 123.0, 300.0, 447.0,
+                                  # at and below the 2^-119 amax floor: zero blocks, tiny blocks, subnormals
+                                  0.0, 2.0**-70, 2.0**-100, 2.0**-119, float.fromhex("0x1.fep-120"), 2.0**-126,
+                                  2.0**-133])
 def test_fp8_codec_all_bf16_values(amax, gpu, oracle):
     """Every finite bf16 value v with |v| <= amax, quantised in blocks whose
     largest magnitude is amax (for amax = 448 the multiplier is exactly 1, so
-    the device conversion of v itself is checked)."""
+    the device conversion of v itself is checked; for amax below 2^-119 the
+    floor sets the scale, and subnormal scales and inputs are exercised)."""
     b = _binding()
     h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
     v = bf16_to_f32(h)

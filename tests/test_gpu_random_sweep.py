@@ -11,6 +11,9 @@ limit.  Then:
     bit-exact; expert stand-in and combine (bf16 and fp32) bit-exact;
   * low-latency dispatch (C = the largest rank): bit-exact against the
     oracle's rectangle; the unordered form on what its contract fixes;
+  * split dispatch and combine (send half, then receive half; the send half
+    on a random SM budget): layout, payload and outputs bit-exact, device
+    error word clear;
   * sender-side partial combine: outputs bit-exact.
 The cases are small so that the oracle finishes each in well under a second."""
 import numpy as np
@@ -115,6 +118,25 @@ def test_random_case(i, gpu, oracle):
     ref32 = oracle.combine(oy, od["tok2row"], o_w, out="f32")
     assert np.array_equal(f32(o32).view(np.uint32), ref32.view(np.uint32))
     assert np.array_equal(bits16(o16), oracle.bf16_from_f32(ref32))
+
+    # split halves: dispatch send (on a random SM budget) -> receive; combine send -> receive
+    rng = np.random.default_rng(c["seed"])
+    ds = b.dispatch_send(x, idx, B, E, fp8=fp8, max_sms=int(rng.choice([0, 1, 7, 38])))
+    b.dispatch_recv(ds, B, E, K)
+    ys = b.expert_scale(ds.recv_x, ds.recv_scale, ds.expert_offsets, E)
+    b.combine_send(ds.workspace, R)
+    os32 = b.combine_recv(ys, ds.tok2row, wg, ds.workspace, R, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    st, code = b.get_device_error(ds.workspace)
+    assert st == 0 and code == 0
+    for key in ("counts", "offsets", "expert_offsets", "tok2row", "row2src"):
+        assert np.array_equal(i32(getattr(ds, key)), od[key]), key
+    if fp8:
+        assert np.array_equal(bytes8(ds.recv_x), od["recv"])
+        assert np.array_equal(f32(ds.recv_scale).view(np.uint32), od["recv_scale"].view(np.uint32))
+    else:
+        assert np.array_equal(bits16(ds.recv_x), od["recv"])
+    assert np.array_equal(f32(os32).view(np.uint32), ref32.view(np.uint32))
 
     # low-latency layouts, chunk cap = the largest rank
     C = max(1, int(B.max()) if B.size else 1)

@@ -9,7 +9,13 @@ copy that nothing ever provides); the product library is built without them.
     limit (about 2 s) with MOE_DEVERR_SCAN_TIMEOUT.
   * MOE_TEST_WITHHOLD_FIRST_LOAD: the scatter warp that takes token 0 arms
     that token's stage barrier but never issues the copy, so its wait ends
-    after its limit with MOE_DEVERR_COPY_TIMEOUT."""
+    after its limit with MOE_DEVERR_COPY_TIMEOUT.
+  * MOE_TEST_WITHHOLD_ARRIVAL_RANK=1 and MOE_TEST_WITHHOLD_READY_RANK=0 (one
+    build): the dispatch send half never announces the copies it stored for
+    rank 1, and the combine send half never publishes rank 0's outputs, so
+    each receive half's wait ends after its limit with
+    MOE_DEVERR_RECV_TIMEOUT; the data itself is in place, so the layout and
+    the sums still equal the oracle's."""
 import ctypes
 import time
 
@@ -21,7 +27,7 @@ pytestmark = pytest.mark.gpu
 
 BF16 = 0
 OK, TIMEOUT = 0, 5
-SCAN_TIMEOUT, COPY_TIMEOUT = 0x4, 0x8
+SCAN_TIMEOUT, COPY_TIMEOUT, RECV_TIMEOUT = 0x4, 0x8, 0x10
 
 
 @pytest.fixture(scope="module")
@@ -33,10 +39,10 @@ def gpu():
     return torch.device("cuda:0")
 
 
-def _hooked_library(tmp_path_factory, define):
+def _hooked_library(tmp_path_factory, *defines):
     from combine_moe_route_gb300 import build
     out = str(tmp_path_factory.mktemp("hooks"))
-    lib = ctypes.CDLL(build.build(out_dir=out, defines=(define,)))
+    lib = ctypes.CDLL(build.build(out_dir=out, defines=defines))
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     lib.moe_dispatch.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.moe_dispatch.restype = i32
@@ -44,6 +50,14 @@ def _hooked_library(tmp_path_factory, define):
     lib.moe_dispatch_workspace_bytes.restype = sz
     lib.moe_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
     lib.moe_get_device_error.restype = i32
+    lib.moe_dispatch_send.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, i32, vp, sz, vp]
+    lib.moe_dispatch_send.restype = i32
+    lib.moe_dispatch_recv.argtypes = [i32, vp, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.moe_dispatch_recv.restype = i32
+    lib.moe_combine_send.argtypes = [i32, vp, sz, vp]
+    lib.moe_combine_send.restype = i32
+    lib.moe_combine_recv.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, i32, vp, sz, vp]
+    lib.moe_combine_recv.restype = i32
     return lib
 
 
@@ -118,3 +132,53 @@ def test_copy_wait_runs_out_and_reports(gpu, oracle, tmp_path_factory):
     t2r = o["tok2row"].cpu().numpy()
     assert np.all((t2r >= -1) & (t2r < idx.numel()))
     _context_still_works(x, idx, B, 8, oracle)
+
+
+def test_receive_halves_run_out_when_a_send_half_withholds(gpu, oracle, tmp_path_factory):
+    lib = _hooked_library(tmp_path_factory, "MOE_TEST_WITHHOLD_ARRIVAL_RANK=1", "MOE_TEST_WITHHOLD_READY_RANK=0")
+    R, E, K, H = 4, 16, 2, 256
+    x, idx, B = _inputs(R, E, K, H, 50, 4, gpu)
+    T = x.shape[0]
+    rows = T * K
+    o = dict(recv=torch.zeros((rows, H), dtype=torch.bfloat16, device=gpu),
+             counts=torch.zeros(E * R, dtype=torch.int32, device=gpu),
+             offsets=torch.zeros(E * R + 1, dtype=torch.int32, device=gpu),
+             eo=torch.zeros(E + 1, dtype=torch.int32, device=gpu),
+             tok2row=torch.zeros(rows, dtype=torch.int32, device=gpu),
+             row2src=torch.zeros(rows, dtype=torch.int32, device=gpu))
+    wsb = lib.moe_dispatch_workspace_bytes(R, E, K, T)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=gpu)
+    stream = torch.cuda.current_stream(gpu).cuda_stream
+    code = ctypes.c_int32(0)
+
+    t0 = time.perf_counter()
+    assert lib.moe_dispatch_send(x.data_ptr(), idx.data_ptr(), R, B.ctypes.data, E, K, H, BF16,
+                                 o["recv"].data_ptr(), None, o["tok2row"].data_ptr(), o["row2src"].data_ptr(), 0,
+                                 ws.data_ptr(), wsb, stream) == OK
+    assert lib.moe_dispatch_recv(R, B.ctypes.data, E, K, o["counts"].data_ptr(), o["offsets"].data_ptr(),
+                                 o["eo"].data_ptr(), ws.data_ptr(), wsb, stream) == OK
+    st = lib.moe_get_device_error(ws.data_ptr(), ctypes.byref(code), stream)   # synchronises
+    dt = time.perf_counter() - t0
+    assert st == TIMEOUT and (code.value & RECV_TIMEOUT), (st, code.value)
+    assert 1.0 < dt < 60.0
+    # the copies themselves were stored: the layout and the rows equal the oracle's
+    ref = oracle.dispatch(x.cpu().view(torch.int16).numpy().view(np.uint16), idx.cpu().numpy(), B, E)
+    assert np.array_equal(o["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(o["tok2row"].cpu().numpy(), ref["tok2row"])
+    assert np.array_equal(o["recv"].cpu().view(torch.int16).numpy().view(np.uint16), ref["recv"])
+
+    # combine: rank 0 never publishes
+    w = torch.rand((T, K), generator=torch.Generator().manual_seed(4)).to(gpu)
+    out = torch.zeros((T, H), dtype=torch.float32, device=gpu)
+    y = o["recv"]
+    t0 = time.perf_counter()
+    assert lib.moe_combine_send(R, ws.data_ptr(), wsb, stream) == OK
+    assert lib.moe_combine_recv(y.data_ptr(), o["tok2row"].data_ptr(), w.data_ptr(), T, K, H, 2, out.data_ptr(), R,
+                                ws.data_ptr(), wsb, stream) == OK
+    st = lib.moe_get_device_error(ws.data_ptr(), ctypes.byref(code), stream)
+    dt = time.perf_counter() - t0
+    assert st == TIMEOUT and (code.value & RECV_TIMEOUT), (st, code.value)
+    assert 1.0 < dt < 60.0
+    refc = oracle.combine(ref["recv"], ref["tok2row"], w.cpu().numpy(), out="f32")
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), refc.view(np.uint32))
+    _context_still_works(x, idx, B, E, oracle)

@@ -120,3 +120,76 @@ def test_workspace_tile_bound():
         T = int(B.sum())
         bound = (T * K + KERNEL_TILE_ITEMS - 1) // KERNEL_TILE_ITEMS + R
         assert tile_off[-1] <= bound
+
+
+# ---------------------------------------------------------------------------
+# the one-kernel path for small batches
+# ---------------------------------------------------------------------------
+
+def _one_kernel_model(idx, B, E, W, sms):
+    """The small-batch kernel's arithmetic: blocks of W warps over contiguous token ranges
+    [g0, g1) (tpb tokens each, at most `sms` blocks); in each block
+        row(i) = start(e) + pre(e) + #{earlier items of the range with expert e},
+    start = exclusive scan of the per-expert totals, pre = the per-expert count of the items
+    before the range; and block b writes source rank b's (then b + grid's ...) layout:
+        offsets[e*R+s] = start(e) + (items of ranks below s routed to e),
+        counts[e*R+s]  = items of rank s routed to e.
+    Also checks every index the kernel forms against its buffer's size."""
+    T, K = idx.shape
+    R = len(B)
+    flat = idx.reshape(-1).astype(np.int64)
+    rank_off = np.concatenate([[0], np.cumsum(np.asarray(B, np.int64))])
+    grid = min(sms, -(-T // W))
+    tpb = -(-T // grid)
+    grid = -(-T // tpb)
+    tot = np.bincount(flat, minlength=E)
+    start = np.concatenate([[0], np.cumsum(tot)])[:E]
+    rows = np.full(T * K, -1, np.int64)
+    offsets = np.full(E * R + 1, -1, np.int64)
+    counts = np.full(E * R, -1, np.int64)
+    for b in range(grid):
+        g0, g1 = b * tpb, min(T, (b + 1) * tpb)
+        assert g1 > g0                                     # every block has a token
+        assert (g1 - g0) * K <= tpb * K                    # the range fits its shared arrays
+        pre = np.bincount(flat[: g0 * K], minlength=E)
+        rng_items = flat[g0 * K: g1 * K]
+        for k, e in enumerate(rng_items):
+            rows[g0 * K + k] = start[e] + pre[e] + int(np.sum(rng_items[:k] == e))
+        for w in range(W):                                 # warp w's tokens g0 + w + it*W
+            n = -(-(g1 - g0 - w) // W) if g1 - g0 > w else 0
+            for it in range(n):
+                assert g0 + w + it * W < g1
+        for s in range(b, R, grid):
+            bef = np.bincount(flat[: rank_off[s] * K], minlength=E)
+            ins = np.bincount(flat[rank_off[s] * K: rank_off[s + 1] * K], minlength=E)
+            for e in range(E):
+                assert e * R + s < E * R
+                offsets[e * R + s] = start[e] + bef[e]
+                counts[e * R + s] = ins[e]
+            if s == R - 1:
+                offsets[E * R] = T * K
+    return rows, counts, offsets, grid
+
+
+ONE_KERNEL_CASES = [
+    # R, E, K, B, W, sms, skew
+    (8, 16, 2, [5, 0, 17, 3, 64, 1, 9, 2], 8, 152, False),
+    (8, 256, 8, [128] * 8, 7, 152, False),                     # DeepSeek-V3 decode
+    (32, 384, 8, list(np.random.default_rng(1).integers(0, 65, 32)), 7, 152, True),
+    (128, 256, 8, list(np.random.default_rng(2).integers(0, 33, 128)), 7, 152, False),
+    (256, 1024, 32, list(np.random.default_rng(3).integers(0, 5, 256)), 3, 7, False),   # ranks > blocks
+    (4, 16, 16, [2049, 0, 5, 1], 8, 152, True),
+    (1, 8, 1, [37], 2, 3, False),
+]
+
+
+@pytest.mark.parametrize("R,E,K,B,W,sms,skew", ONE_KERNEL_CASES)
+def test_one_kernel_rows_are_the_oracle_layout(oracle, R, E, K, B, W, sms, skew):
+    rng = np.random.default_rng(R + E + K + W)
+    T = int(np.sum(B))
+    idx = _routing(T, E, K, rng, skew)
+    d = oracle.dispatch(np.zeros((T, 8), np.uint16), idx, B, E)
+    rows, counts, offsets, _ = _one_kernel_model(idx, B, E, W, sms)
+    assert np.array_equal(rows, d["tok2row"])
+    assert np.array_equal(counts, d["counts"])
+    assert np.array_equal(offsets, d["offsets"])

@@ -4,10 +4,13 @@ a serving loop that must not allocate on its hot path).  It uses the library's
 static device scratch instead of a workspace.
 
 Called here through the C ABI with ctypes; every output must equal, bit for
-bit, what moe_dispatch (with a caller workspace) produces for the same input
--- the same bar the other dispatch parity tests use -- on two calls in a row,
-the second with different sizes, so that state left in the shared scratch by
-the first call cannot leak into the second.  This file is collected last."""
+bit, both the CPU oracle's dispatch and what moe_dispatch (with a caller
+workspace) produces for the same input -- the same bar the other dispatch
+parity tests use -- on two calls in a row, the second with different sizes, so
+that state left in the shared scratch by the first call cannot leak into the
+second.  One case needs a workspace within a few KB of the scratch's size, so
+the end of the array (where the scan output lies) is used and compared; one
+just past it is refused with MOE_ERR_WORKSPACE.  This file is collected last."""
 import ctypes
 
 import numpy as np
@@ -69,18 +72,44 @@ def _case(R, E, K, H, B, seed, dev):
     inp = wl.random_shape_inputs(R, E, K, H, B, seed=seed)
     x = inp["x"].to(dev)
     rng = np.random.default_rng(seed)
-    idx = np.stack([rng.permutation(E)[:K] for _ in range(inp["T"])]).astype(np.int32).reshape(inp["T"], K)
+    # K distinct experts per token: the K smallest of E uniform keys
+    idx = np.argpartition(rng.random((inp["T"], E), dtype=np.float32), K - 1, axis=1)[:, :K]
+    idx = np.ascontiguousarray(idx.astype(np.int32)).reshape(inp["T"], K)
     return x, torch.from_numpy(idx).to(dev), np.asarray(inp["B"], np.int32)
 
 
-def test_noalloc_matches_dispatch_two_calls_in_a_row(lib):
+def _near_full_B():
+    """8 ranks of 256*m + 1 tokens (one item past a whole number of 2048-item tiles, so the
+    call's tile count is one short of the bound the workspace size is computed from), with
+    E = 256 and K = 8: the workspace is within 3 KB of the 1 MiB scratch."""
+    m = [63, 63, 63, 63, 63, 63, 62, 62]
+    return [256 * v + 1 for v in m]
+
+
+def _compare_with_oracle(got, x, idx, B, E, fp8):
+    import oracle
+    from combine_moe_route_gb300 import workloads as wl
+    ref = oracle.dispatch(wl.bf16_bits(x.cpu()), idx.cpu().numpy(), B, E, fp8=fp8)
+    for key in ("counts", "offsets", "expert_offsets", "tok2row", "row2src"):
+        assert np.array_equal(got[key].cpu().numpy(), ref[key]), key
+    if fp8:
+        assert np.array_equal(got["recv"].cpu().numpy(), ref["recv"])
+        assert np.array_equal(got["scale"].cpu().numpy().view(np.uint32), ref["recv_scale"].view(np.uint32))
+    else:
+        assert np.array_equal(got["recv"].cpu().numpy().view(np.uint16), ref["recv"])
+
+
+def test_noalloc_matches_oracle_and_dispatch_on_calls_in_a_row(lib):
     dev = torch.device("cuda:0")
     stream = torch.cuda.current_stream(dev).cuda_stream
     cases = [
         dict(R=8, E=256, K=8, H=7168, B=[128, 0, 77, 300, 5, 128, 64, 1], fp8=True, seed=21),
+        dict(R=8, E=256, K=8, H=16, B=_near_full_B(), fp8=False, seed=23),
         dict(R=4, E=16, K=2, H=256, B=[9, 1, 0, 33], fp8=False, seed=22),
     ]
-    for c in cases:   # two calls in a row on the shared scratch, different sizes and payloads
+    near = lib.moe_dispatch_workspace_bytes(8, 256, 8, sum(_near_full_B()))
+    assert (1 << 20) - 3 * 1024 <= near <= (1 << 20)
+    for c in cases:   # calls in a row on the shared scratch, different sizes and payloads
         x, idx, B = _case(c["R"], c["E"], c["K"], c["H"], c["B"], c["seed"], dev)
         T, K, H, E, R = x.shape[0], c["K"], c["H"], c["E"], c["R"]
         got = _outputs(T, K, H, E, R, c["fp8"], dev)
@@ -95,9 +124,25 @@ def test_noalloc_matches_dispatch_two_calls_in_a_row(lib):
             if a.dtype == torch.float32:
                 a, b = a.view(torch.int32), b.view(torch.int32)
             assert torch.equal(a, b), key
+        _compare_with_oracle(got, x, idx, B, E, c["fp8"])
         # the layout is a complete one: every routed copy placed exactly once
         assert int(got["offsets"][-1]) == T * K
         assert torch.equal(torch.sort(got["row2src"]).values, torch.arange(T * K, device=dev, dtype=torch.int32))
+        del got, ref
+        torch.cuda.empty_cache()
+
+
+def test_noalloc_refuses_a_call_just_past_its_scratch(lib):
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    Bl = _near_full_B()
+    Bl[0] += 256                          # one more tile: the bound passes 1 MiB
+    assert lib.moe_dispatch_workspace_bytes(8, 256, 8, sum(Bl)) > (1 << 20)
+    x, idx, B = _case(8, 256, 8, 16, Bl, 24, dev)
+    got = _outputs(x.shape[0], 8, 16, 256, 8, False, dev)
+    assert _call(lib, True, x, idx, B, 256, False, got, stream) == WORKSPACE
+    torch.cuda.synchronize()
+    assert bool((got["counts"] == -7).all()) and bool((got["tok2row"] == -7).all())   # nothing was enqueued
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
