@@ -20,9 +20,11 @@
 // is staged once in shared memory by a bulk copy and written by bulk copies
 // straight into its K destination rows.
 //
-// Three kernels, stream-ordered (the second and third launched with
-// programmatic stream serialization, so each starts while its predecessor
-// finishes and waits only where it reads the predecessor's output):
+// Batches of more than MOE_SMALL_DISPATCH_ITEMS (token, slot) items run three
+// kernels, stream-ordered (the second and third launched with programmatic
+// stream serialization, so each starts while its predecessor finishes and
+// waits only where it reads the predecessor's output); smaller ones run the
+// one-kernel path of section 4 below, with the same layout:
 //  1. tile histogram: the items (g, j) of one rank are cut into tiles of
 //     kTileItems consecutive items.  Each warp counts its run of 256 items
 //     into a warp-private shared histogram; lanes holding the same expert are
@@ -666,10 +668,15 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
 //      (pre), and, for the source rank s = b (then b + grid, ...), the items
 //      of the ranks below s (bef) and of rank s (ins);
 //   C. tot is scanned into start(e); the block writes rank s's layout --
-//      counts[e*R+s] = ins(e), offsets[e*R+s] = start(e) + bef(e) -- and ranks
-//      each of its own items among the earlier ones of its range;
-//   D. its warps scatter their tokens (one warp per token, two bulk-copy
-//      stages, in-place FP8) as the scatter kernel does.
+//      counts[e*R+s] = ins(e), offsets[e*R+s] = start(e) + bef(e);
+//   D. chunk by chunk (ctok tokens, at most kSmallChunkItems items), the
+//      block ranks each item of the chunk among the earlier items of the same
+//      expert (pre counts those before the chunk and grows after each one),
+//      and its warps scatter the chunk's tokens (one warp per token, two
+//      bulk-copy stages, in-place FP8) as the scatter kernel does.
+// A block normally holds a handful of tokens and one chunk; the chunks keep
+// shared memory and the ranking bounded when a capped SM budget gives each
+// block many.
 // The kernel runs behind a one-block kernel that clears the workspace header
 // and signals (programmatic stream serialization); it waits for that kernel
 // before it first touches either.  The send half of the split dispatch
@@ -677,6 +684,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
 // reads them, instead of the counts / offsets / expert_offsets outputs.
 constexpr int kSmallMaxWarps = 8;
 constexpr int kSmallStages = 2;
+constexpr int kSmallChunkItems = 512;
 #ifndef MOE_SMALL_DISPATCH_ITEMS
 #define MOE_SMALL_DISPATCH_ITEMS 32768   // T*K up to which a dispatch takes the one-kernel path
 #endif
@@ -696,13 +704,23 @@ struct SmallArgs {
     int32_t *arrive;           // send half: copies landed per destination rank, else null
     int T, E, K, H;
     int tpb;                   // tokens per block
+    int ctok;                  // tokens per chunk: a multiple of the warps per block
+    int stages;                // bulk-copy stages per warp: 2, or 1 when no warp has a second token
 };
 
+// Tokens per chunk for W warps and top-K: the most whole rounds of W tokens
+// whose items fit kSmallChunkItems (one round at least; W * K <= 256).
+__host__ __device__ inline int small_chunk_tokens(int W, int K) {
+    const int rounds = kSmallChunkItems / K / W;
+    return W * (rounds > 0 ? rounds : 1);
+}
+
 // Bytes of dynamic shared memory of the one-kernel dispatch for W warps.
-__host__ __device__ inline size_t small_smem_bytes(int W, int H, bool fp8, int E, int R, int tpb, int K, bool send) {
-    size_t b = (size_t)W * kSmallStages * scatter_stage_bytes(H, fp8);
+__host__ __device__ inline size_t small_smem_bytes(int W, int stages, int H, bool fp8, int E, int R, int K,
+                                                   bool send) {
+    size_t b = (size_t)W * stages * scatter_stage_bytes(H, fp8);
     b += (size_t)4 * E * 4;                   // tot, pre, bef, ins
-    b += (size_t)2 * tpb * K * 4;             // the range's expert ids and rows
+    b += (size_t)2 * small_chunk_tokens(W, K) * K * 4;   // a chunk's expert ids and rows
     if (send) b += (size_t)W * R * 4;         // per-warp arrival tallies
     return b;
 }
@@ -719,7 +737,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bars[kSmallMaxWarps][kSmallStages];
     __shared__ int s_total;
-    constexpr int S = kSmallStages;
+    const int S = a.stages;   // 1 or 2 (kSmallStages)
     const int W = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -735,15 +753,15 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
     const long long g0 = (long long)blockIdx.x * a.tpb;
     const long long g1 = min(g0 + (long long)a.tpb, (long long)T);
     const int ntok = (int)(g1 - g0);
-    const int my_n = ntok > warp ? (ntok - warp + W - 1) / W : 0;   // tokens g0 + warp + i*W
+    const int my_n = ntok > warp ? (ntok - warp + W - 1) / W : 0;   // tokens g0 + warp + it*W
 
     int32_t *tot = reinterpret_cast<int32_t *>(smem + (size_t)W * S * stage_bytes);
     int32_t *pre = tot + E;
     int32_t *bef = pre + E;
     int32_t *ins = bef + E;
-    int32_t *s_idx = ins + E;                 // [tpb*K] expert ids of the block's items
-    int32_t *s_row = s_idx + a.tpb * K;       // [tpb*K] their rows
-    int32_t *s_arr = send ? s_row + a.tpb * K + warp * R : nullptr;
+    int32_t *s_idx = ins + E;                 // [ctok*K] expert ids of the chunk's items
+    int32_t *s_row = s_idx + a.ctok * K;      // [ctok*K] their rows
+    int32_t *s_arr = send ? s_row + a.ctok * K + warp * R : nullptr;
     auto stage = [&](int it) { return smem + ((size_t)warp * S + (it % S)) * stage_bytes; };
 
     // A. stage the first rows
@@ -753,62 +771,258 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
         for (int it = 0; it < S && it < my_n; ++it) {
             const long long g = g0 + warp + (long long)it * W;
             mbar_arrive_expect_tx(&bars[warp][it], in_bytes);
+#ifdef MOE_TEST_WITHHOLD_FIRST_LOAD
+            // Test builds only: token 0's stage is armed but never filled, so its
+            // bounded barrier wait runs out.
+            if (g == 0) continue;
+#endif
             bulk_load(stage(it), a.x + g * H, in_bytes, &bars[warp][it]);
         }
     }
 
-    // B. counts
+    // B. counts; the first chunk's expert ids are fetched first, so that they
+    // arrive while the block counts
+    const int cn_first = min(a.ctok, ntok);
+    for (int k = threadIdx.x; k < cn_first * K; k += blockDim.x) s_idx[k] = __ldg(a.topk_idx + g0 * K + k);
     for (int i = threadIdx.x; i < 4 * E; i += blockDim.x) tot[i] = 0;
     if (send)
         for (int r = lane; r < R; r += 32) s_arr[r] = 0;
     __syncthreads();
     const long long n_all = (long long)T * K;
     const long long pb = g0 * K;
+    // Each thread takes 16 consecutive items per round and issues all their
+    // loads (four 16-byte loads when the ids are 16-byte aligned) before the
+    // first shared-memory atomic, so a round costs one L2 round trip.
+    const bool vec_ids = (reinterpret_cast<uintptr_t>(a.topk_idx) & 15) == 0;
     auto count_pass = [&](long long lim, long long mlo, long long mhi, bool all) {
-        for (long long i = threadIdx.x; i < lim; i += blockDim.x) {
-            const int e = __ldg(a.topk_idx + i);
-            if ((unsigned)e >= (unsigned)E) continue;   // reported in D
-            if (all) {
-                atomicAdd(&tot[e], 1);
-                if (i < pb) atomicAdd(&pre[e], 1);
+        constexpr int kU = 16;
+        for (long long base = (long long)threadIdx.x * kU; base < lim; base += (long long)blockDim.x * kU) {
+            int ev[kU];
+            if (vec_ids && base + kU <= lim) {
+#pragma unroll
+                for (int q = 0; q < kU / 4; ++q) {
+                    const int4 v = __ldg(reinterpret_cast<const int4 *>(a.topk_idx + base) + q);
+                    ev[4 * q] = v.x;
+                    ev[4 * q + 1] = v.y;
+                    ev[4 * q + 2] = v.z;
+                    ev[4 * q + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) ev[u] = (base + u < lim) ? __ldg(a.topk_idx + base + u) : -1;
             }
-            if (i < mlo)
-                atomicAdd(&bef[e], 1);
-            else if (i < mhi)
-                atomicAdd(&ins[e], 1);
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int e = ev[u];
+                const long long i = base + u;
+                if ((unsigned)e >= (unsigned)E) continue;   // out of range (reported in D) or past lim
+                if (all) {
+                    atomicAdd(&tot[e], 1);
+                    if (i < pb) atomicAdd(&pre[e], 1);
+                }
+                if (i < mlo)
+                    atomicAdd(&bef[e], 1);
+                else if (i < mhi)
+                    atomicAdd(&ins[e], 1);
+            }
         }
     };
+    // The first pass needs four per-expert counts: all items (tot), those
+    // before g0 (pre), before rank s (bef) and inside rank s (ins).  Sorting
+    // the three boundaries g0*K, rank_off[s]*K, rank_off[s+1]*K cuts the items
+    // into four contiguous segments; each item adds to its segment's histogram
+    // (one shared-memory atomic instead of up to four), and the four counts
+    // are sums of leading segments.
     int s_meta = blockIdx.x;
-    if (s_meta < R)
-        count_pass(n_all, (long long)rt.rank_off[s_meta] * K, (long long)rt.rank_off[s_meta + 1] * K, true);
-    else
-        count_pass(n_all, 0, 0, true);
-    for (int k = threadIdx.x; k < ntok * K; k += blockDim.x) s_idx[k] = __ldg(a.topk_idx + pb + k);
-    __syncthreads();
-
-    // C. start(e): exclusive scan of tot, in place (warp 0; E <= 1024)
-    if (warp == 0) {
-        const int per = (E + 31) >> 5;
-        int sum = 0;
-        for (int k = 0; k < per; ++k) {
-            const int e = lane * per + k;
-            if (e < E) sum += tot[e];
-        }
-        const int incl = warp_inclusive_scan(sum);
-        int run = incl - sum;
-        for (int k = 0; k < per; ++k) {
-            const int e = lane * per + k;
-            if (e < E) {
-                const int c = tot[e];
-                tot[e] = run;
-                run += c;
+    {
+        const long long mlo = s_meta < R ? (long long)rt.rank_off[s_meta] * K : 0;
+        const long long mhi = s_meta < R ? (long long)rt.rank_off[s_meta + 1] * K : 0;
+        long long c0 = pb, c1 = mlo, c2 = mhi;   // sorted into c0 <= c1 <= c2
+        if (c0 > c1) { const long long t = c0; c0 = c1; c1 = t; }
+        if (c1 > c2) { const long long t = c1; c1 = c2; c2 = t; }
+        if (c0 > c1) { const long long t = c0; c0 = c1; c1 = t; }
+        int32_t *seg = tot;   // [4][E]: tot, pre, bef, ins reused as the segment histograms
+        constexpr int kU = 16;   // items per thread per round, all loads issued before the atomics
+        for (long long base = (long long)threadIdx.x * kU; base < n_all; base += (long long)blockDim.x * kU) {
+            int ev[kU];
+            if (vec_ids && base + kU <= n_all) {
+#pragma unroll
+                for (int q = 0; q < kU / 4; ++q) {
+                    const int4 v = __ldg(reinterpret_cast<const int4 *>(a.topk_idx + base) + q);
+                    ev[4 * q] = v.x;
+                    ev[4 * q + 1] = v.y;
+                    ev[4 * q + 2] = v.z;
+                    ev[4 * q + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) ev[u] = (base + u < n_all) ? __ldg(a.topk_idx + base + u) : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int e = ev[u];
+                const long long i = base + u;
+                if ((unsigned)e >= (unsigned)E) continue;   // out of range (reported in D) or past the end
+                const int sg = (i >= c0) + (i >= c1) + (i >= c2);
+                atomicAdd(&seg[sg * E + e], 1);
             }
         }
-        if (lane == 31) s_total = incl;
+        __syncthreads();
+        // segment k covers [c_{k-1}, c_k): the items below a boundary are the
+        // segments up to the boundary's place among c0 <= c1 <= c2
+        const int r_pre = pb == c0 ? 0 : (pb == c1 ? 1 : 2);
+        const int r_lo = mlo == c0 ? 0 : (mlo == c1 ? 1 : 2);
+        const int r_hi = mhi == c0 ? 0 : (mhi == c1 ? 1 : 2);
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            const int run0 = seg[e];
+            const int run1 = run0 + seg[E + e];
+            const int run2 = run1 + seg[2 * E + e];
+            const int run3 = run2 + seg[3 * E + e];
+            auto below = [&](int r) { return r == 0 ? run0 : (r == 1 ? run1 : run2); };
+            const int lo = below(r_lo);
+            tot[e] = run3;
+            pre[e] = below(r_pre);
+            bef[e] = lo;
+            ins[e] = below(r_hi) - lo;
+        }
+    }
+    __syncthreads();
+
+    // C. start(e): exclusive scan of tot, in place, by the whole block: thread t
+    // takes the consecutive entries [t*q, t*q + q) (q = ceil(E / threads), at
+    // most 5), then warp sums, then the warps' totals
+    {
+        __shared__ int s_wsum[kSmallMaxWarps];
+        const int q = (E + blockDim.x - 1) / blockDim.x;
+        const int e0 = threadIdx.x * q;
+        int mine = 0;
+        for (int k = 0; k < q; ++k)
+            if (e0 + k < E) mine += tot[e0 + k];
+        const int incl = warp_inclusive_scan(mine);
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        int before = 0, all = 0;
+        for (int w = 0; w < W; ++w) {
+            const int ws = s_wsum[w];
+            if (w < warp) before += ws;
+            all += ws;
+        }
+        int run = before + incl - mine;
+        for (int k = 0; k < q; ++k)
+            if (e0 + k < E) {
+                const int c = tot[e0 + k];
+                tot[e0 + k] = run;
+                run += c;
+            }
+        if (threadIdx.x == 0) s_total = all;
     }
     __syncthreads();
     const int total = s_total;
-    // the layout of source ranks blockIdx.x, blockIdx.x + grid, ...
+    // D. chunks.  The header (error word) and signals are cleared by the kernel
+    // ahead; this kernel waits for it (griddepcontrol.wait, a no-op once it has
+    // completed) only right before it first writes either -- an error bit, or
+    // the send half's announcements at the end -- so the stores never wait.
+    auto report = [&](int bits) {
+        pdl_wait();
+        set_device_error(a.err, bits);
+    };
+    int failed_at = -1;
+    int it = 0;   // this warp's position in its token sequence g0 + warp + it*W
+    for (long long c0 = g0; c0 < g1; c0 += a.ctok) {
+        const int cn = (int)min((long long)a.ctok, g1 - c0);
+        const long long cb = c0 * K;
+        __syncthreads();   // the previous chunk's rows are read, and pre counts every item before c0
+        if (c0 != g0) {    // the first chunk's ids were fetched in B
+            for (int k = threadIdx.x; k < cn * K; k += blockDim.x) s_idx[k] = __ldg(a.topk_idx + cb + k);
+            __syncthreads();
+        }
+        // row = start + the earlier items of the same expert: before the chunk, then inside it
+        for (int k = threadIdx.x; k < cn * K; k += blockDim.x) {
+            const int e = s_idx[k];
+            int row = -1;
+            if ((unsigned)e < (unsigned)E) {
+                int rr = 0;
+                for (int k2 = 0; k2 < k; ++k2) rr += (s_idx[k2] == e) ? 1 : 0;
+                row = tot[e] + pre[e] + rr;
+            }
+            s_row[k] = row;
+        }
+        __syncthreads();
+        for (int k = threadIdx.x; k < cn * K; k += blockDim.x) {   // pre for the next chunk
+            const int e = s_idx[k];
+            if ((unsigned)e < (unsigned)E) atomicAdd(&pre[e], 1);
+        }
+        for (; failed_at < 0 && it < my_n; ++it) {
+            const long long g = g0 + warp + (long long)it * W;
+            if (g >= c0 + cn) break;   // the warp's next token is in the next chunk
+            const uint32_t parity = (uint32_t)((it / S) & 1);
+            unsigned char *buf = stage(it);
+            const int k0 = (int)(g - c0) * K;
+            int my_dest = -1;
+            {
+                int e = -1, row = -1;
+                if (lane < K) {
+                    const long long i = g * K + lane;
+                    e = s_idx[k0 + lane];
+                    row = s_row[k0 + lane];
+                    if ((unsigned)e >= (unsigned)E) {
+                        report(MOE_DEVERR_EXPERT_RANGE);
+                        e = -1;
+                        row = -1;
+                    }
+                    a.tok2row[i] = row;
+                    if (row >= 0) {
+                        a.row2src[row] = (int32_t)i;
+                        if (send) my_dest = e / L;
+                    }
+                }
+                int dup = 0;
+                for (int j = 0; j < K; ++j) {
+                    const int ej = __shfl_sync(0xffffffffu, e, j);
+                    if (lane < j && e >= 0 && e == ej) dup = 1;
+                }
+                if (__any_sync(0xffffffffu, dup) && lane == 0) report(MOE_DEVERR_DUPLICATE);
+            }
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][it % S], parity));
+            if (!ok) {
+                if (lane == 0) report(MOE_DEVERR_COPY_TIMEOUT);
+                failed_at = it;
+                break;
+            }
+            if (my_dest >= 0) atomicAdd(&s_arr[my_dest], 1);   // stored below
+            float *sc = reinterpret_cast<float *>(buf + (size_t)H * 2);
+            if (kFp8) quantize_stage(buf, H, lane);
+            __syncwarp();
+            if (lane == 0) {
+                for (int j = 0; j < K; ++j) {
+                    const int row = s_row[k0 + j];
+                    if (row < 0 || (unsigned)s_idx[k0 + j] >= (unsigned)E) continue;
+                    bulk_store(static_cast<unsigned char *>(a.recv_x) + (size_t)row * recv_pitch, buf, out_bytes);
+                    if (scale_bulk) bulk_store(a.recv_scale + (size_t)row * nblk, sc, (uint32_t)nblk * 4u);
+                }
+                bulk_commit();
+            }
+            if (kFp8 && !scale_bulk) {
+                for (int t = lane; t < K * nblk; t += 32) {
+                    const int j = t / nblk;
+                    const int b = t - j * nblk;
+                    const int row = s_row[k0 + j];
+                    if (row >= 0 && (unsigned)s_idx[k0 + j] < (unsigned)E) a.recv_scale[(size_t)row * nblk + b] = sc[b];
+                }
+            }
+            // refill the previous token's stage with token it - 1 + S once its stores have read it
+            if (lane == 0 && S >= 2 && it >= 1 && it - 1 + S < my_n) {
+                bulk_wait_read<1>();
+                const int nxt = it - 1 + S;
+                const long long gn = g0 + warp + (long long)nxt * W;
+                mbar_arrive_expect_tx(&bars[warp][nxt % S], in_bytes);
+                bulk_load(stage(nxt), a.x + gn * H, in_bytes, &bars[warp][nxt % S]);
+            }
+            __syncwarp();
+        }
+    }   // chunks
+    // the layout of source ranks blockIdx.x, blockIdx.x + grid, ... (written after the
+    // scatter: nothing in this kernel reads it, and the stores start sooner)
     for (; s_meta < R; s_meta += gridDim.x) {
         if (s_meta != (int)blockIdx.x) {   // a further rank: count again
             __syncthreads();
@@ -837,89 +1051,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
             }
         }
     }
-    // rows of the block's items: start + earlier tokens (before the range, then inside it)
-    for (int k = threadIdx.x; k < ntok * K; k += blockDim.x) {
-        const int e = s_idx[k];
-        int row = -1;
-        if ((unsigned)e < (unsigned)E) {
-            int rr = 0;
-            for (int k2 = 0; k2 < k; ++k2) rr += (s_idx[k2] == e) ? 1 : 0;
-            row = tot[e] + pre[e] + rr;
-        }
-        s_row[k] = row;
-    }
-    __syncthreads();
-
-    // D. scatter; the header (error word) and signals are cleared by the kernel ahead
-    pdl_wait();
-    int failed_at = -1;
-    for (int it = 0; failed_at < 0 && it < my_n; ++it) {
-        const uint32_t parity = (uint32_t)((it / S) & 1);
-        unsigned char *buf = stage(it);
-        const long long g = g0 + warp + (long long)it * W;
-        const int k0 = (int)(g - g0) * K;
-        int my_dest = -1;
-        {
-            int e = -1, row = -1;
-            if (lane < K) {
-                const long long i = g * K + lane;
-                e = s_idx[k0 + lane];
-                row = s_row[k0 + lane];
-                if ((unsigned)e >= (unsigned)E) {
-                    set_device_error(a.err, MOE_DEVERR_EXPERT_RANGE);
-                    e = -1;
-                    row = -1;
-                }
-                a.tok2row[i] = row;
-                if (row >= 0) {
-                    a.row2src[row] = (int32_t)i;
-                    if (send) my_dest = e / L;
-                }
-            }
-            int dup = 0;
-            for (int j = 0; j < K; ++j) {
-                const int ej = __shfl_sync(0xffffffffu, e, j);
-                if (lane < j && e >= 0 && e == ej) dup = 1;
-            }
-            if (__any_sync(0xffffffffu, dup) && lane == 0) set_device_error(a.err, MOE_DEVERR_DUPLICATE);
-        }
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][it % S], parity));
-        if (!ok) {
-            if (lane == 0) set_device_error(a.err, MOE_DEVERR_COPY_TIMEOUT);
-            failed_at = it;
-            break;
-        }
-        if (my_dest >= 0) atomicAdd(&s_arr[my_dest], 1);   // stored below
-        float *sc = reinterpret_cast<float *>(buf + (size_t)H * 2);
-        if (kFp8) quantize_stage(buf, H, lane);
-        __syncwarp();
-        if (lane == 0) {
-            for (int j = 0; j < K; ++j) {
-                const int row = s_row[k0 + j];
-                if (row < 0 || (unsigned)s_idx[k0 + j] >= (unsigned)E) continue;
-                bulk_store(static_cast<unsigned char *>(a.recv_x) + (size_t)row * recv_pitch, buf, out_bytes);
-                if (scale_bulk) bulk_store(a.recv_scale + (size_t)row * nblk, sc, (uint32_t)nblk * 4u);
-            }
-            bulk_commit();
-        }
-        if (kFp8 && !scale_bulk) {
-            for (int t = lane; t < K * nblk; t += 32) {
-                const int j = t / nblk;
-                const int b = t - j * nblk;
-                const int row = s_row[k0 + j];
-                if (row >= 0 && (unsigned)s_idx[k0 + j] < (unsigned)E) a.recv_scale[(size_t)row * nblk + b] = sc[b];
-            }
-        }
-        // refill the previous token's stage with token it - 1 + S once its stores have read it
-        if (lane == 0 && it >= 1 && it - 1 + S < my_n) {
-            bulk_wait_read<1>();
-            const int nxt = it - 1 + S;
-            const long long gn = g0 + warp + (long long)nxt * W;
-            mbar_arrive_expect_tx(&bars[warp][nxt % S], in_bytes);
-            bulk_load(stage(nxt), a.x + gn * H, in_bytes, &bars[warp][nxt % S]);
-        }
-        __syncwarp();
-    }
+    pdl_wait();   // this grid ends after the kernel ahead, whatever path it took
     if (lane == 0) {
         if (failed_at >= 0) {
             // let every load this warp issued land before the block's shared memory goes away
@@ -935,6 +1067,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
         }
     }
     if (send) {
+        pdl_wait();   // the arrival counters were cleared by the kernel ahead
         __syncwarp();
         for (int r = lane; r < R; r += 32) {
             const int c = s_arr[r];
@@ -1096,7 +1229,7 @@ static cudaError_t launch_dispatch_small(const void *x, const int32_t *topk_idx,
     if (max_sms > 0 && max_sms < sms) sms = max_sms;
     // warps per block: as many (up to 8) as two stages of rows per warp leave room for
     const size_t smem_cap = 227 * 1024 - 1024;
-    int W = 0, tpb = 0;
+    int W = 0, tpb = 0, stages = 0;
     long long grid = 0;
     size_t smem = 0;
     for (int w = kSmallMaxWarps; w >= 1 && W == 0; --w) {
@@ -1104,10 +1237,12 @@ static cudaError_t launch_dispatch_small(const void *x, const int32_t *topk_idx,
         if (gr > sms) gr = sms;
         const int tp = (int)((T + gr - 1) / gr);
         gr = (T + tp - 1) / tp;   // every block has at least one token
-        const size_t sm = small_smem_bytes(w, H, fp8, E, rt.R, tp, K, send);
+        const int st = tp > w ? kSmallStages : 1;   // one stage when every warp has one token
+        const size_t sm = small_smem_bytes(w, st, H, fp8, E, rt.R, K, send);
         if (sm <= smem_cap) {
             W = w;
             tpb = tp;
+            stages = st;
             grid = gr;
             smem = sm;
         }
@@ -1139,6 +1274,8 @@ static cudaError_t launch_dispatch_small(const void *x, const int32_t *topk_idx,
     a.K = K;
     a.H = H;
     a.tpb = tpb;
+    a.ctok = small_chunk_tokens(W, K);
+    a.stages = stages;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(W * 32);

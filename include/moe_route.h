@@ -112,7 +112,8 @@ MOE_API const char *moe_strerror(int status);
  *            descending logit; equal logits go to the smaller id (+0 and -0
  *            count as equal).
  *   topk_w   device, fp32 [T, K]     out: softmax over the K selected logits,
- *            w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), summed in j order.
+ *            w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), in fp32 (CUDA expf,
+ *            the K terms summed pairwise across the warp, one IEEE division).
  * Errors: MOE_ERR_INVALID_ARG for T < 0, E or K out of range, NULL pointers
  * with T > 0; MOE_ERR_CUDA if the launch fails.
  */

@@ -7,7 +7,7 @@ copy that nothing ever provides); the product library is built without them.
   * MOE_TEST_WITHHOLD_SCAN_BLOCK=0: the first lookback-scan block never
     publishes its status, so the second block's lookback wait ends after its
     limit (about 2 s) with MOE_DEVERR_SCAN_TIMEOUT.
-  * MOE_TEST_WITHHOLD_FIRST_LOAD: the scatter warp that takes token 0 arms
+  * MOE_TEST_WITHHOLD_FIRST_LOAD: the warp that takes token 0 (in either dispatch path) arms
     that token's stage barrier but never issues the copy, so its wait ends
     after its limit with MOE_DEVERR_COPY_TIMEOUT.
   * MOE_TEST_WITHHOLD_ARRIVAL_RANK=1 and MOE_TEST_WITHHOLD_READY_RANK=0 (one

@@ -128,10 +128,11 @@ def test_workspace_tile_bound():
 
 def _one_kernel_model(idx, B, E, W, sms):
     """The small-batch kernel's arithmetic: blocks of W warps over contiguous token ranges
-    [g0, g1) (tpb tokens each, at most `sms` blocks); in each block
-        row(i) = start(e) + pre(e) + #{earlier items of the range with expert e},
+    [g0, g1) (tpb tokens each, at most `sms` blocks), each range taken in chunks of whole
+    rounds of W tokens (at most 512 items); in each chunk
+        row(i) = start(e) + pre(e) + #{earlier items of the chunk with expert e},
     start = exclusive scan of the per-expert totals, pre = the per-expert count of the items
-    before the range; and block b writes source rank b's (then b + grid's ...) layout:
+    before the chunk; and block b writes source rank b's (then b + grid's ...) layout:
         offsets[e*R+s] = start(e) + (items of ranks below s routed to e),
         counts[e*R+s]  = items of rank s routed to e.
     Also checks every index the kernel forms against its buffer's size."""
@@ -150,15 +151,34 @@ def _one_kernel_model(idx, B, E, W, sms):
     for b in range(grid):
         g0, g1 = b * tpb, min(T, (b + 1) * tpb)
         assert g1 > g0                                     # every block has a token
-        assert (g1 - g0) * K <= tpb * K                    # the range fits its shared arrays
         pre = np.bincount(flat[: g0 * K], minlength=E)
-        rng_items = flat[g0 * K: g1 * K]
-        for k, e in enumerate(rng_items):
-            rows[g0 * K + k] = start[e] + pre[e] + int(np.sum(rng_items[:k] == e))
+        ctok = W * max(1, 512 // K // W)                   # chunk: whole rounds of W tokens, <= 512 items
+        assert ctok * K <= max(512, W * K) and ctok % W == 0
+        for c0 in range(g0, g1, ctok):
+            chunk = flat[c0 * K: min(g1, c0 + ctok) * K]
+            for k, e in enumerate(chunk):
+                rows[c0 * K + k] = start[e] + pre[e] + int(np.sum(chunk[:k] == e))
+            pre = pre + np.bincount(chunk, minlength=E)
         for w in range(W):                                 # warp w's tokens g0 + w + it*W
             n = -(-(g1 - g0 - w) // W) if g1 - g0 > w else 0
             for it in range(n):
                 assert g0 + w + it * W < g1
+        # the kernel's first pass: one histogram per segment between the sorted
+        # boundaries g0*K, rank_off[s]*K, rank_off[s+1]*K (s = b when b < R), and
+        # the four counts as sums of leading segments
+        mlo = rank_off[b] * K if b < R else 0
+        mhi = rank_off[b + 1] * K if b < R else 0
+        c = sorted([int(g0 * K), int(mlo), int(mhi)])
+        seg = np.zeros((4, E), np.int64)
+        for i, e in enumerate(flat):
+            seg[(i >= c[0]) + (i >= c[1]) + (i >= c[2]), e] += 1
+        run = np.cumsum(seg, axis=0)
+        place = lambda v: c.index(int(v))
+        assert np.array_equal(run[3], tot)
+        assert np.array_equal(run[place(g0 * K)], np.bincount(flat[: g0 * K], minlength=E))
+        if b < R:
+            assert np.array_equal(run[place(mlo)], np.bincount(flat[:mlo], minlength=E))
+            assert np.array_equal(run[place(mhi)] - run[place(mlo)], np.bincount(flat[mlo:mhi], minlength=E))
         for s in range(b, R, grid):
             bef = np.bincount(flat[: rank_off[s] * K], minlength=E)
             ins = np.bincount(flat[rank_off[s] * K: rank_off[s + 1] * K], minlength=E)
@@ -180,6 +200,8 @@ ONE_KERNEL_CASES = [
     (256, 1024, 32, list(np.random.default_rng(3).integers(0, 5, 256)), 3, 7, False),   # ranks > blocks
     (4, 16, 16, [2049, 0, 5, 1], 8, 152, True),
     (1, 8, 1, [37], 2, 3, False),
+    (8, 64, 8, [300, 0, 257, 512, 1, 255, 256, 64], 8, 1, True),   # one block: many chunks
+    (4, 32, 3, [700, 5, 0, 900], 6, 2, False),                     # chunks of 6*28 tokens
 ]
 
 

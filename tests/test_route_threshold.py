@@ -1,6 +1,9 @@
 """The bound behind the route kernel's candidate filter (CPU only).
 
-The kernel keeps one warp per token; lane l holds the keys of experts l, l+32, ... .
+The kernel keeps one warp per token; lane l holds the keys of experts l, l+32, ...
+(or, with 16-byte loads when E is 32 * NPL and a multiple of 128, experts
+128q + 4l .. 128q + 4l + 3); the bound holds for any split of the experts among the
+lanes, and both splits are checked.
 Its threshold tau is the upper 27 bits of the K-th largest of the 32 lane maxima, each
 with its low 5 bits replaced by the tag 31 - l (a lane without keys contributes 0), and
 every eligible key >= tau becomes a candidate.  The selection is exact only if the
@@ -16,11 +19,18 @@ def _keys(f):
     return np.where((u >> 31) == 1, (~u) & 0xFFFFFFFF, u | 0x80000000)
 
 
-def _tagged_tau(k, K):
+def _lane_of(e, E, vec):
+    return (e % 128) // 4 if vec else e % 32
+
+
+def _tagged_tau(k, K, vec=False):
     E = k.size
     lanes = np.zeros((32, -(-E // 32)), np.uint64)
+    fill = np.zeros(32, np.int64)
     for e in range(E):
-        lanes[e % 32, e // 32] = k[e]
+        l = _lane_of(e, E, vec)
+        lanes[l, fill[l]] = k[e]
+        fill[l] += 1
     lmax = lanes.max(axis=1)
     v = np.where(lmax > 0, (lmax & ~np.uint64(31)) | (31 - np.arange(32)).astype(np.uint64), 0)
     top = 0
@@ -30,9 +40,11 @@ def _tagged_tau(k, K):
     return top & ~31
 
 
-@pytest.mark.parametrize("E,K", [(256, 8), (32, 32), (40, 33), (9, 3), (1024, 32), (384, 8), (64, 1)])
+@pytest.mark.parametrize("E,K,vec", [(256, 8, False), (32, 32, False), (40, 33, False), (9, 3, False),
+                                     (1024, 32, False), (384, 8, False), (64, 1, False),
+                                     (256, 8, True), (128, 4, True), (384, 8, True), (1024, 32, True)])
 @pytest.mark.parametrize("kind", ["normal", "ties", "denormal"])
-def test_candidates_hold_the_top_k(E, K, kind):
+def test_candidates_hold_the_top_k(E, K, vec, kind):
     rng = np.random.default_rng(E * 100 + K)
     for _ in range(150):
         if kind == "normal":
@@ -43,7 +55,7 @@ def test_candidates_hold_the_top_k(E, K, kind):
             f = rng.integers(-3, 4, E) * np.float32(1e-45)
         k = _keys(np.asarray(f, np.float32))
         order = np.lexsort((np.arange(E), -k.astype(np.int64)))
-        tau = _tagged_tau(k, K)
+        tau = _tagged_tau(k, K, vec)
         cand = np.flatnonzero((k != 0) & (k >= tau))
         assert set(order[:K].tolist()) <= set(cand.tolist())
 
@@ -57,6 +69,7 @@ def test_fewer_lanes_than_k_admits_every_key():
 def test_random_rows_admit_few_candidates():
     # DeepSeek-V3 router shape: about K plus one candidates per row on N(0, 1) logits
     rng = np.random.default_rng(11)
-    n = [int(((k := _keys(rng.standard_normal(256).astype(np.float32))) >= _tagged_tau(k, 8)).sum())
-         for _ in range(400)]
-    assert 8 <= min(n) and np.mean(n) < 10 and max(n) <= 64
+    for vec in (False, True):
+        n = [int(((k := _keys(rng.standard_normal(256).astype(np.float32))) >= _tagged_tau(k, 8, vec)).sum())
+             for _ in range(400)]
+        assert 8 <= min(n) and np.mean(n) < 10 and max(n) <= 64
