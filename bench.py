@@ -752,95 +752,100 @@ def run_ours(args, world, rank, local):
     dc_us_max = max_over_ranks(dc_us, world, dev)
     step_ms_max = max_over_ranks(total_ms / args.steps, world, dev)
 
-    # the same calls with the L2 left warm (no flush between them), outside the timed region
-    uev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(20)]
-    for e in uev:
-        e[0].record(stream)
-        b.dispatch(x, idx, B, E, fp8=w.fp8, out=d)
-        e[1].record(stream)
-        e[2].record(stream)
-        b.combine(y, d.tok2row, wts, out=out)
-        e[3].record(stream)
-    torch.cuda.synchronize()
-    unflushed = {"dispatch": statistics.mean(e[0].elapsed_time(e[1]) for e in uev[2:]) * 1e3,
-                 "combine": statistics.mean(e[2].elapsed_time(e[3]) for e in uev[2:]) * 1e3,
-                 "note": "back-to-back calls without an L2 flush; the expert stand-in does not run between them"}
+    # everything after the timed region (warm-L2 calls, end to end through host memory, the
+    # "next" rows, the other workloads) is skipped with --kernels-only, which profiling uses
+    unflushed = e2e_us = e2e_serial_us = x_h = lg_h = out_h = None
+    next_rows, others = {}, {}
+    if not args.kernels_only:
+        # the same calls with the L2 left warm (no flush between them), outside the timed region
+        uev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(20)]
+        for e in uev:
+            e[0].record(stream)
+            b.dispatch(x, idx, B, E, fp8=w.fp8, out=d)
+            e[1].record(stream)
+            e[2].record(stream)
+            b.combine(y, d.tok2row, wts, out=out)
+            e[3].record(stream)
+        torch.cuda.synchronize()
+        unflushed = {"dispatch": statistics.mean(e[0].elapsed_time(e[1]) for e in uev[2:]) * 1e3,
+                     "combine": statistics.mean(e[2].elapsed_time(e[3]) for e in uev[2:]) * 1e3,
+                     "note": "back-to-back calls without an L2 flush; the expert stand-in does not run between them"}
 
-    # end to end through the public API: pinned host inputs -> device -> layer -> pinned host output.
-    # Serial: one layer after another on one stream.  Pipelined (HostLayerPipeline): the input copy
-    # of layer i+1 and the output copy of layer i-1 overlap the compute of layer i.
-    from combine_moe_route_gb300.pipeline import HostLayerPipeline
-    x_h = inp["x"].pin_memory()
-    lg_h = torch.from_numpy(inp["logits"]).pin_memory()
-    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(3, min(args.steps, 20))
+        # end to end through the public API: pinned host inputs -> device -> layer -> pinned host output.
+        # Serial: one layer after another on one stream.  Pipelined (HostLayerPipeline): the input copy
+        # of layer i+1 and the output copy of layer i-1 overlap the compute of layer i.
+        from combine_moe_route_gb300.pipeline import HostLayerPipeline
+        x_h = inp["x"].pin_memory()
+        lg_h = torch.from_numpy(inp["logits"]).pin_memory()
+        out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        e2e_steps = max(3, min(args.steps, 20))
 
-    def e2e_step():
-        x.copy_(x_h, non_blocking=True)
-        logits.copy_(lg_h, non_blocking=True)
-        b.route_topk(logits, K, topk_idx=idx, topk_w=wts)
-        b.dispatch(x, idx, B, E, fp8=w.fp8, out=d)
-        b.expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E, out=y)
-        b.combine(y, d.tok2row, wts, out=out)
-        out_h.copy_(out, non_blocking=True)
+        def e2e_step():
+            x.copy_(x_h, non_blocking=True)
+            logits.copy_(lg_h, non_blocking=True)
+            b.route_topk(logits, K, topk_idx=idx, topk_w=wts)
+            b.dispatch(x, idx, B, E, fp8=w.fp8, out=d)
+            b.expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E, out=y)
+            b.combine(y, d.tok2row, wts, out=out)
+            out_h.copy_(out, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_serial_us = max_over_ranks(e0.elapsed_time(e1) * 1e3 / e2e_steps, world, dev)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_serial_us = max_over_ranks(e0.elapsed_time(e1) * 1e3 / e2e_steps, world, dev)
 
-    pipe = HostLayerPipeline(B, E, K, H, fp8=w.fp8, device=dev, depth=2)
-    outs_h = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    for i in range(2):
-        pipe.submit(x_h, lg_h, outs_h[i % 2])
-    pipe.synchronize()
-    barrier(world)
-    p0 = torch.cuda.Event(enable_timing=True)
-    p1 = torch.cuda.Event(enable_timing=True)
-    p0.record(pipe.h2d)
-    for i in range(e2e_steps):
-        pipe.submit(x_h, lg_h, outs_h[i % 2])
-    p1.record(pipe.d2h)
-    pipe.synchronize()
-    e2e_us = max_over_ranks(p0.elapsed_time(p1) * 1e3 / e2e_steps, world, dev)
-    del pipe
+        pipe = HostLayerPipeline(B, E, K, H, fp8=w.fp8, device=dev, depth=2)
+        outs_h = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        for i in range(2):
+            pipe.submit(x_h, lg_h, outs_h[i % 2])
+        pipe.synchronize()
+        barrier(world)
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(pipe.h2d)
+        for i in range(e2e_steps):
+            pipe.submit(x_h, lg_h, outs_h[i % 2])
+        p1.record(pipe.d2h)
+        pipe.synchronize()
+        e2e_us = max_over_ranks(p0.elapsed_time(p1) * 1e3 / e2e_steps, world, dev)
+        del pipe
 
-    # the "next" rows, each timed on its own after the main region (not part of value)
-    next_rows = {}
-    if E % 8 == 0 and K <= 4 * (E // 8):
-        g_idx = torch.empty_like(idx)
-        g_w = torch.empty_like(wts)
+        # the "next" rows, each timed on its own after the main region (not part of value)
+        next_rows = {}
+        if E % 8 == 0 and K <= 4 * (E // 8):
+            g_idx = torch.empty_like(idx)
+            g_w = torch.empty_like(wts)
 
-        def grouped():
-            b.route_topk_grouped(logits, K, 8, 4, topk_idx=g_idx, topk_w=g_w)
+            def grouped():
+                b.route_topk_grouped(logits, K, 8, 4, topk_idx=g_idx, topk_w=g_w)
 
-        us = time_call(grouped, stream, reps=50)
-        next_rows["route_grouped_G8_M4"] = {"us": us, "GBps": route_bytes(T, E, K) / (us * 1e-6) / 1e9}
+            us = time_call(grouped, stream, reps=50)
+            next_rows["route_grouped_G8_M4"] = {"us": us, "GBps": route_bytes(T, E, K) / (us * 1e-6) / 1e9}
 
-    next_rows.update(measure_partial_combine(b, y, d, idx, wts, out, E, w.R, K, H, T, stream, flush))
-    next_rows.update(measure_eager_layers(dev, stream))
-    peak_gbs, _ = measured_peaks()
-    split = {}
-    if args.tokens_per_rank is None:
-        split[args.workload] = measure_split_halves(args.workload, dev, stream, flush)
-        if args.workload != "dsv3_decode":
-            split["dsv3_decode"] = measure_split_halves("dsv3_decode", dev, stream, flush)
-    next_rows["split_halves"] = split
-    # every other workload, each on its own (parity cases of the same path, not the headline)
-    others = {}
-    if args.tokens_per_rank is None and not args.headline_only:
-        for name in ("toy", "dsv3_decode", "kimi_decode", "wide_ep_decode", "dsv3_prefill"):
-            if name != args.workload:
-                others[name] = measure_workload(name, dev, stream, flush, peak_gbs)
-                torch.cuda.empty_cache()
+        next_rows.update(measure_partial_combine(b, y, d, idx, wts, out, E, w.R, K, H, T, stream, flush))
+        next_rows.update(measure_eager_layers(dev, stream))
+        peak_gbs, _ = measured_peaks()
+        split = {}
+        if args.tokens_per_rank is None:
+            split[args.workload] = measure_split_halves(args.workload, dev, stream, flush)
+            if args.workload != "dsv3_decode":
+                split["dsv3_decode"] = measure_split_halves("dsv3_decode", dev, stream, flush)
+        next_rows["split_halves"] = split
+        # every other workload, each on its own (parity cases of the same path, not the headline)
+        others = {}
+        if args.tokens_per_rank is None and not args.headline_only:
+            for name in ("toy", "dsv3_decode", "kimi_decode", "wide_ep_decode", "dsv3_prefill"):
+                if name != args.workload:
+                    others[name] = measure_workload(name, dev, stream, flush, peak_gbs)
+                    torch.cuda.empty_cache()
 
     # correctness of what was timed: the last step's outputs equal the first layer's
     st, code = b.get_device_error(d.workspace)
@@ -899,14 +904,17 @@ def run_ours(args, world, rank, local):
         "p50_us": {"dispatch": statistics.median(disp_ms) * 1e3, "combine": statistics.median(comb_ms) * 1e3},
         "p10_p90_us": {"dispatch": pct(disp_ms), "combine": pct(comb_ms)},
         "unflushed_us": unflushed,
-        "e2e": {"value": replica_value(e2e_us, world), "unit": UNIT,
+        "e2e": None if e2e_us is None else {
+                "value": replica_value(e2e_us, world), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_h.numel() * 2 + lg_h.numel() * 4),
                 "d2h_bytes_per_step": int(out_h.numel() * 2),
                 "serial_us": replica_value(e2e_serial_us, world),
                 "note": "per layer: tokens and logits host->device, route + dispatch + expert stand-in + combine, "
                         "output device->host, through the package API; value: HostLayerPipeline (copies of "
                         "neighbouring layers overlap the compute), serial_us: one stream"},
-        "gpu_launches": 6 * args.steps,
+        # per step: route, dispatch (prep + one kernel up to 32768 (token, slot) items, else
+        # histogram + scan + scatter), expert stand-in, combine
+        "gpu_launches": (3 + (2 if T * K <= 32768 else 3)) * args.steps,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"], "window": clk["window"]},
         "cpu_baseline": cpu,
@@ -928,6 +936,9 @@ def main():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--headline-only", action="store_true",
                    help="skip the per-workload measurements of the other four layers")
+    p.add_argument("--kernels-only", action="store_true",
+                   help="only the timed steps (no end-to-end, next-row or other-workload measurements): "
+                        "a small device footprint for profiling")
     p.add_argument("--tokens-per-rank", type=int, default=None,
                    help="override B (every rank) for a smaller case of the workload, e.g. for ncu captures")
     args = p.parse_args()

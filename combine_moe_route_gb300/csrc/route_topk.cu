@@ -277,159 +277,6 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
     }
 }
 
-// Two tokens per warp, for plain routing with K <= 16: lanes 0-15 take one
-// token and lanes 16-31 the next, each half with E/16 logits per lane (four
-// consecutive experts per lane per 64 when E = 16 * NPL2 is a multiple of 64,
-// else expert gl + 16 i).  The selection is the one above, with every
-// collective -- the K threshold rounds, the prefix sum, the broadcasts, the
-// butterfly -- run by each half on its own member mask, so one warp
-// instruction serves two tokens.  The threshold tags are 4 bits (15 - lane in
-// the half).
-template <bool kVec>
-__device__ __forceinline__ int pair_slot_expert(int gl, int i) {
-    return kVec ? ((i >> 2) << 6) + (gl << 2) + (i & 3) : gl + 16 * i;
-}
-
-template <int NPL2, bool kVec>
-__global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_pair_kernel(const float *__restrict__ logits,
-                                                                                       int T, int E, int K,
-                                                                                       int32_t *__restrict__ topk_idx,
-                                                                                       float *__restrict__ topk_w) {
-    constexpr int kWarps = RouteShape::kWarps;
-    __shared__ unsigned long long s_cand[kWarps][2][kMaxCandidates];
-    __shared__ unsigned long long s_win[kWarps][2][16];
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int half = lane >> 4;
-    const int gl = lane & 15;
-    const unsigned gmask = half ? 0xffff0000u : 0x0000ffffu;
-    const long long stride = (long long)gridDim.x * kWarps * 2;
-    long long gw = ((long long)blockIdx.x * kWarps + warp) * 2;   // the pair's first token
-    if (gw >= T) return;
-    unsigned long long *cand = s_cand[warp][half];
-    unsigned long long *win = s_win[warp][half];
-
-    auto load = [&](long long g, float (&v)[NPL2]) {
-        const bool live = g < T;
-        if (kVec) {
-#pragma unroll
-            for (int q = 0; q < NPL2 / 4; ++q) {
-                float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (live) f = __ldg(reinterpret_cast<const float4 *>(logits + g * (long long)E + q * 64 + gl * 4));
-                v[4 * q] = f.x;
-                v[4 * q + 1] = f.y;
-                v[4 * q + 2] = f.z;
-                v[4 * q + 3] = f.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < NPL2; ++i) {
-                const int e = gl + 16 * i;
-                v[i] = (live && e < E) ? __ldg(logits + g * (long long)E + e) : 0.0f;
-            }
-        }
-    };
-    float nxt[NPL2];
-    load(gw + half, nxt);
-    for (;; gw += stride) {
-        const long long g = gw + half;
-        const bool live = g < T;
-        uint32_t ek[NPL2];   // keys; 0 = no expert (every real key is > 0)
-        uint32_t lmax = 0u;
-#pragma unroll
-        for (int i = 0; i < NPL2; ++i) {
-            ek[i] = (live && pair_slot_expert<kVec>(gl, i) < E) ? ordered_key(nxt[i]) : 0u;
-            lmax = max(lmax, ek[i]);
-        }
-        const bool more = gw + stride < T;
-        if (more) load(gw + stride + half, nxt);
-
-        // threshold: as in route_topk_kernel, over this half's 16 lane maxima
-        uint32_t v = lmax ? ((lmax & ~15u) | (uint32_t)(15 - gl)) : 0u;
-        uint32_t top = 0u;
-        for (int k = 0; k < K; ++k) {
-            top = __reduce_max_sync(gmask, v);
-            if (v == top) v = 0u;
-        }
-        const uint32_t tau = top & ~15u;
-        uint32_t cm = 0u;
-#pragma unroll
-        for (int i = 0; i < NPL2; ++i)
-            if (ek[i] != 0u && ek[i] >= tau) cm |= 1u << i;
-        const int cnt = __popc(cm);
-        int incl = cnt;
-#pragma unroll
-        for (int off = 1; off < 16; off <<= 1) {
-            const int o = __shfl_up_sync(gmask, incl, off, 16);
-            if (gl >= off) incl += o;
-        }
-        const int n = __shfl_sync(gmask, incl, 15, 16);
-
-        int my_e = 0;
-        uint32_t my_key = 0;
-        if (n <= kMaxCandidates) {
-            int pos = incl - cnt;
-#pragma unroll
-            for (int i = 0; i < NPL2; ++i)
-                if (cm & (1u << i))
-                    cand[pos++] = ((unsigned long long)ek[i] << 32) |
-                                  (unsigned long long)(~(uint32_t)pair_slot_expert<kVec>(gl, i));
-            __syncwarp(gmask);
-            for (int c = gl; c < n; c += 16) {
-                const unsigned long long me = cand[c];
-                int r = 0;
-#pragma unroll 4
-                for (int m = 0; m < n; ++m) r += (cand[m] > me) ? 1 : 0;
-                if (r < K) win[r] = me;
-            }
-            __syncwarp(gmask);
-            if (gl < K) {
-                const unsigned long long wv = win[gl];
-                my_key = (uint32_t)(wv >> 32);
-                my_e = (int)~(uint32_t)wv;
-            }
-        } else {
-            for (int k = 0; k < K; ++k) {
-                uint32_t bk = 0u;
-                int bi = -1;
-#pragma unroll
-                for (int i = 0; i < NPL2; ++i)
-                    if (ek[i] > bk) {
-                        bk = ek[i];
-                        bi = i;
-                    }
-                const uint32_t kmax = __reduce_max_sync(gmask, bk);
-                uint32_t c = 0xffffffffu;
-#pragma unroll
-                for (int i = 0; i < NPL2; ++i)
-                    if (i == bi && bk == kmax) c = (uint32_t)pair_slot_expert<kVec>(gl, i);
-                const uint32_t e_win = __reduce_min_sync(gmask, c);
-#pragma unroll
-                for (int i = 0; i < NPL2; ++i)
-                    if ((uint32_t)pair_slot_expert<kVec>(gl, i) == e_win) ek[i] = 0u;
-                if (gl == k) {
-                    my_e = (int)e_win;
-                    my_key = kmax;
-                }
-            }
-        }
-
-        // softmax over the half's K winners (lane gl < K of the half holds winner gl)
-        const float my_l = key_to_float(my_key);
-        const float m = __shfl_sync(gmask, my_l, 0, 16);
-        const float ex = (gl < K) ? expf(my_l - m) : 0.0f;
-        float sum = ex;
-#pragma unroll
-        for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(gmask, sum, off, 16);
-        if (live && gl < K) {
-            topk_idx[g * K + gl] = my_e;
-            topk_w[g * K + gl] = ex / sum;
-        }
-        if (!more) break;
-        __syncwarp();   // cand / win are refilled for the next pair
-    }
-}
-
 #ifndef MOE_ROUTE_WAVES
 #define MOE_ROUTE_WAVES 2   // resident waves of blocks; each warp then walks its share of the tokens
 #endif
@@ -461,44 +308,9 @@ static cudaError_t launch_npl(const float *logits, int T, int E, int K, int G, i
     return cudaGetLastError();
 }
 
-#ifndef MOE_ROUTE_PAIR
-#define MOE_ROUTE_PAIR 0   // 1: two tokens per warp for plain routing with E <= 256 and K <= 16
-#endif
-
-template <int NPL2, bool kVec>
-static cudaError_t launch_pair(const float *logits, int T, int E, int K, int32_t *topk_idx, float *topk_w,
-                               cudaStream_t stream) {
-    static std::atomic<int> per_sm_cache[64];
-    int dev = 0;
-    cudaError_t ce = cudaGetDevice(&dev);
-    if (ce != cudaSuccess) return ce;
-    if (dev < 0 || dev >= 64) dev = 0;
-    int per_sm = per_sm_cache[dev].load(std::memory_order_relaxed);
-    if (per_sm == 0) {
-        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_topk_pair_kernel<NPL2, kVec>,
-                                                           RouteShape::kWarps * 32, 0);
-        if (ce != cudaSuccess) return ce;
-        if (per_sm < 1) per_sm = 1;
-        per_sm_cache[dev].store(per_sm, std::memory_order_relaxed);
-    }
-    long long grid = ((long long)T + 2 * RouteShape::kWarps - 1) / (2 * RouteShape::kWarps);
-    const long long cap = (long long)device_sm_count() * per_sm * MOE_ROUTE_WAVES;
-    if (grid > cap) grid = cap;
-    route_topk_pair_kernel<NPL2, kVec><<<(unsigned)grid, RouteShape::kWarps * 32, 0, stream>>>(logits, T, E, K,
-                                                                                               topk_idx, topk_w);
-    return cudaGetLastError();
-}
-
 template <int NPL>
 static cudaError_t launch_layout(const float *logits, int T, int E, int K, int G, int M, int32_t *topk_idx,
                                  float *topk_w, cudaStream_t stream) {
-    if constexpr (NPL == 8) {   // E in (128, 256]
-        if (MOE_ROUTE_PAIR && G <= 1 && K <= 16) {
-            if (E == 256 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0)
-                return launch_pair<16, true>(logits, T, E, K, topk_idx, topk_w, stream);
-            return launch_pair<16, false>(logits, T, E, K, topk_idx, topk_w, stream);
-        }
-    }
     // 16-byte loads: plain routing over exactly 32 * NPL experts, a multiple of 128, aligned rows
     if constexpr (NPL % 4 == 0) {
         if (G <= 1 && E == 32 * NPL && (reinterpret_cast<uintptr_t>(logits) & 15) == 0)
