@@ -912,9 +912,9 @@ def run_ours(args, world, rank, local):
                 "note": "per layer: tokens and logits host->device, route + dispatch + expert stand-in + combine, "
                         "output device->host, through the package API; value: HostLayerPipeline (copies of "
                         "neighbouring layers overlap the compute), serial_us: one stream"},
-        # per step: route, dispatch (prep + one kernel up to 32768 (token, slot) items, else
+        # per step: route, dispatch (prep + one kernel up to 16384 (token, slot) items, else
         # histogram + scan + scatter), expert stand-in, combine
-        "gpu_launches": (3 + (2 if T * K <= 32768 else 3)) * args.steps,
+        "gpu_launches": (3 + (2 if T * K <= 16384 else 3)) * args.steps,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
                    "samples": clk["samples"], "window": clk["window"]},
         "cpu_baseline": cpu,

@@ -686,7 +686,7 @@ constexpr int kSmallMaxWarps = 8;
 constexpr int kSmallStages = 2;
 constexpr int kSmallChunkItems = 512;
 #ifndef MOE_SMALL_DISPATCH_ITEMS
-#define MOE_SMALL_DISPATCH_ITEMS 32768   // T*K up to which a dispatch takes the one-kernel path
+#define MOE_SMALL_DISPATCH_ITEMS 16384   // T*K up to which a dispatch takes the one-kernel path
 #endif
 
 struct SmallArgs {
@@ -706,6 +706,7 @@ struct SmallArgs {
     int tpb;                   // tokens per block
     int ctok;                  // tokens per chunk: a multiple of the warps per block
     int stages;                // bulk-copy stages per warp: 2, or 1 when no warp has a second token
+    int stage_ids;             // 1: the whole topk_idx is staged in shared memory by one bulk copy
 };
 
 // Tokens per chunk for W warps and top-K: the most whole rounds of W tokens
@@ -725,6 +726,12 @@ __host__ __device__ inline size_t small_smem_bytes(int W, int stages, int H, boo
     return b;
 }
 
+// Offset and bytes of the staged routing table (after everything above, 16-byte aligned).
+__host__ __device__ inline size_t small_ids_offset(int W, int stages, int H, bool fp8, int E, int R, int K,
+                                                    bool send) {
+    return (small_smem_bytes(W, stages, H, fp8, E, R, K, send) + 15) & ~(size_t)15;
+}
+
 __global__ void dispatch_prep_kernel(int32_t *__restrict__ header, int32_t *__restrict__ signal, int nsignal) {
     pdl_launch_dependents();
     for (int i = threadIdx.x; i < (int)(kWsHeader / 4); i += blockDim.x) header[i] = 0;
@@ -736,6 +743,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
                                                                              const __grid_constant__ RankTable rt) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bars[kSmallMaxWarps][kSmallStages];
+    __shared__ __align__(8) uint64_t bar_ids;
     __shared__ int s_total;
     const int S = a.stages;   // 1 or 2 (kSmallStages)
     const int W = blockDim.x >> 5;
@@ -764,7 +772,16 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
     int32_t *s_arr = send ? s_row + a.ctok * K + warp * R : nullptr;
     auto stage = [&](int it) { return smem + ((size_t)warp * S + (it % S)) * stage_bytes; };
 
-    // A. stage the first rows
+    // A. stage the routing table (when it fits) and the first rows
+    const long long n_all = (long long)T * K;
+    int32_t *s_items = reinterpret_cast<int32_t *>(smem + small_ids_offset(W, S, H, kFp8, E, R, K, send));
+    const uint32_t ids_bulk = (uint32_t)((n_all * 4) & ~15ll);   // the bulk copy's whole 16-byte units
+    if (threadIdx.x == 0 && a.stage_ids) {
+        mbar_init(&bar_ids, 1);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bar_ids, ids_bulk);
+        bulk_load(s_items, a.topk_idx, ids_bulk, &bar_ids);
+    }
     if (lane == 0) {
         for (int st = 0; st < S; ++st) mbar_init(&bars[warp][st], 1);
         fence_proxy_async_smem();
@@ -787,8 +804,16 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
     for (int i = threadIdx.x; i < 4 * E; i += blockDim.x) tot[i] = 0;
     if (send)
         for (int r = lane; r < R; r += 32) s_arr[r] = 0;
-    __syncthreads();
-    const long long n_all = (long long)T * K;
+    // the routing table from shared memory when its copy landed (the last
+    // few ids beyond the copy's 16-byte units are read here), else from global
+    bool staged = false;
+    if (a.stage_ids) {
+        __syncthreads();   // bar_ids is initialised
+        staged = mbar_wait_bounded(&bar_ids, 0u);
+        for (long long i = ids_bulk / 4 + threadIdx.x; i < n_all; i += blockDim.x) s_items[i] = __ldg(a.topk_idx + i);
+    }
+    staged = __syncthreads_and(staged) != 0;
+    const int32_t *ids = staged ? s_items : a.topk_idx;
     const long long pb = g0 * K;
     // Each thread takes 16 consecutive items per round and issues all their
     // loads (four 16-byte loads when the ids are 16-byte aligned) before the
@@ -801,7 +826,8 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
             if (vec_ids && base + kU <= lim) {
 #pragma unroll
                 for (int q = 0; q < kU / 4; ++q) {
-                    const int4 v = __ldg(reinterpret_cast<const int4 *>(a.topk_idx + base) + q);
+                    const int4 v = staged ? reinterpret_cast<const int4 *>(ids + base)[q]
+                                          : __ldg(reinterpret_cast<const int4 *>(a.topk_idx + base) + q);
                     ev[4 * q] = v.x;
                     ev[4 * q + 1] = v.y;
                     ev[4 * q + 2] = v.z;
@@ -809,7 +835,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
                 }
             } else {
 #pragma unroll
-                for (int u = 0; u < kU; ++u) ev[u] = (base + u < lim) ? __ldg(a.topk_idx + base + u) : -1;
+                for (int u = 0; u < kU; ++u) ev[u] = (base + u < lim) ? ids[base + u] : -1;
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
@@ -848,7 +874,8 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
             if (vec_ids && base + kU <= n_all) {
 #pragma unroll
                 for (int q = 0; q < kU / 4; ++q) {
-                    const int4 v = __ldg(reinterpret_cast<const int4 *>(a.topk_idx + base) + q);
+                    const int4 v = staged ? reinterpret_cast<const int4 *>(ids + base)[q]
+                                          : __ldg(reinterpret_cast<const int4 *>(a.topk_idx + base) + q);
                     ev[4 * q] = v.x;
                     ev[4 * q + 1] = v.y;
                     ev[4 * q + 2] = v.z;
@@ -856,7 +883,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
                 }
             } else {
 #pragma unroll
-                for (int u = 0; u < kU; ++u) ev[u] = (base + u < n_all) ? __ldg(a.topk_idx + base + u) : -1;
+                for (int u = 0; u < kU; ++u) ev[u] = (base + u < n_all) ? ids[base + u] : -1;
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
@@ -1050,6 +1077,12 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
                 a.expert_offsets[E] = total;
             }
         }
+    }
+    if (a.stage_ids && !staged && threadIdx.x == 0) {
+        // the routing table's copy did not land in time (the ids were read from
+        // global memory): report it, and let it land before shared memory goes away
+        report(MOE_DEVERR_COPY_TIMEOUT);
+        (void)mbar_wait_bounded(&bar_ids, 0u);
     }
     pdl_wait();   // this grid ends after the kernel ahead, whatever path it took
     if (lane == 0) {
@@ -1248,6 +1281,10 @@ static cudaError_t launch_dispatch_small(const void *x, const int32_t *topk_idx,
         }
     }
     if (W == 0) return cudaErrorInvalidConfiguration;   // unreachable for H <= MOE_MAX_HIDDEN
+    // the routing table staged in shared memory when it fits beside the stages
+    const size_t ids_need = small_ids_offset(W, stages, H, fp8, E, rt.R, K, send) + (((size_t)T * K * 4 + 15) & ~(size_t)15);
+    const int stage_ids = ((reinterpret_cast<uintptr_t>(topk_idx) & 15) == 0 && T * K >= 4 && ids_need <= smem_cap) ? 1 : 0;
+    if (stage_ids) smem = ids_need;
     const void *kfn = fp8 ? (const void *)dispatch_small_kernel<true> : (const void *)dispatch_small_kernel<false>;
     int per_sm = 0;
     cudaError_t ce;
@@ -1276,6 +1313,7 @@ static cudaError_t launch_dispatch_small(const void *x, const int32_t *topk_idx,
     a.tpb = tpb;
     a.ctok = small_chunk_tokens(W, K);
     a.stages = stages;
+    a.stage_ids = stage_ids;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(W * 32);
