@@ -780,7 +780,12 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
         mbar_init(&bar_ids, 1);
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bar_ids, ids_bulk);
+#ifndef MOE_TEST_WITHHOLD_IDS_COPY
         bulk_load(s_items, a.topk_idx, ids_bulk, &bar_ids);
+#endif
+        // (test builds with MOE_TEST_WITHHOLD_IDS_COPY arm the barrier but never
+        // issue the copy, so its bounded wait runs out and the ids come from
+        // global memory)
     }
     if (lane == 0) {
         for (int st = 0; st < S; ++st) mbar_init(&bars[warp][st], 1);

@@ -10,6 +10,10 @@ copy that nothing ever provides); the product library is built without them.
   * MOE_TEST_WITHHOLD_FIRST_LOAD: the warp that takes token 0 (in either dispatch path) arms
     that token's stage barrier but never issues the copy, so its wait ends
     after its limit with MOE_DEVERR_COPY_TIMEOUT.
+  * MOE_TEST_WITHHOLD_IDS_COPY: the one-kernel dispatch arms the barrier of
+    its routing-table copy into shared memory but never issues the copy; each
+    block's wait ends after its limit, the block counts from global memory
+    instead, and the dispatch is still exact, with MOE_DEVERR_COPY_TIMEOUT.
   * MOE_TEST_WITHHOLD_ARRIVAL_RANK=1 and MOE_TEST_WITHHOLD_READY_RANK=0 (one
     build): the dispatch send half never announces the copies it stored for
     rank 1, and the combine send half never publishes rank 0's outputs, so
@@ -182,3 +186,18 @@ def test_receive_halves_run_out_when_a_send_half_withholds(gpu, oracle, tmp_path
     refc = oracle.combine(ref["recv"], ref["tok2row"], w.cpu().numpy(), out="f32")
     assert np.array_equal(out.cpu().numpy().view(np.uint32), refc.view(np.uint32))
     _context_still_works(x, idx, B, E, oracle)
+
+
+def test_routing_table_copy_runs_out_and_the_dispatch_falls_back(gpu, oracle, tmp_path_factory):
+    lib = _hooked_library(tmp_path_factory, "MOE_TEST_WITHHOLD_IDS_COPY")
+    # 8 ranks x 128 tokens, top-8 of 256: the one-kernel path, table staged in shared memory
+    x, idx, B = _inputs(8, 256, 8, 512, 128, 5, gpu)
+    st, code, dt, o = _dispatch_with(lib, x, idx, B, 256, gpu)
+    assert st == TIMEOUT and (code & COPY_TIMEOUT), (st, code)
+    assert 1.0 < dt < 60.0
+    ref = oracle.dispatch(x.cpu().view(torch.int16).numpy().view(np.uint16), idx.cpu().numpy(), B, 256)
+    for key, name in (("counts", "counts"), ("offsets", "offsets"), ("eo", "expert_offsets"),
+                      ("tok2row", "tok2row"), ("row2src", "row2src")):
+        assert np.array_equal(o[key].cpu().numpy(), ref[name]), key
+    assert np.array_equal(o["recv"].cpu().view(torch.int16).numpy().view(np.uint16), ref["recv"])
+    _context_still_works(x, idx, B, 256, oracle)
