@@ -108,9 +108,11 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
         if (!kPrefetch) load_row<NPL, kVec>(logits + g * (long long)E, E, lane, nxt);
         uint32_t key[NPL];
         uint32_t avail = 0;   // bit i: slot i holds an eligible expert
+        // (the 16-byte-load layout runs only for plain routing over exactly
+        // E = 32 * NPL experts, so there every slot is in range and eligible)
 #pragma unroll
         for (int i = 0; i < NPL; ++i) {
-            if (slot_expert<kVec>(lane, i) < E) {
+            if (kVec || slot_expert<kVec>(lane, i) < E) {
                 key[i] = ordered_key(nxt[i]);
                 avail |= 1u << i;
             } else {
@@ -120,7 +122,8 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
         const bool more = g + stride < T;
         if (kPrefetch && more) load_row<NPL, kVec>(logits + (g + stride) * (long long)E, E, lane, nxt);
 
-        if (G > 1) {   // keep the M best groups; the experts of the others leave the race
+        // keep the M best groups; the experts of the others leave the race
+        if (!kVec && G > 1) {
             const int gs = E / G;
             // group of slot i, when every slot lies inside one group (group size a
             // multiple of 32): slots 0..spg-1 are group 0, and so on
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
 #pragma unroll
         for (int i = 0; i < NPL; ++i) {
             // the plain top-K keeps every in-range slot; key[i] is already 0 past E
-            ek[i] = (G <= 1 || (avail & (1u << i))) ? key[i] : 0u;
+            ek[i] = (kVec || G <= 1 || (avail & (1u << i))) ? key[i] : 0u;
             lmax = max(lmax, ek[i]);
         }
         uint32_t v = lmax ? ((lmax & ~31u) | (uint32_t)(31 - lane)) : 0u;
@@ -192,11 +195,12 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
             top = __reduce_max_sync(0xffffffffu, v);
             if (v == top) v = 0u;   // the one lane holding top (top = 0: nothing left, no change)
         }
-        const uint32_t tau = top & ~31u;
+        // at least 1, so that one compare also drops the ineligible slots (key 0)
+        const uint32_t tau = max(top & ~31u, 1u);
         uint32_t cm = 0u;   // bit i: slot i is a candidate
 #pragma unroll
         for (int i = 0; i < NPL; ++i)
-            if (ek[i] != 0u && ek[i] >= tau) cm |= 1u << i;
+            if (ek[i] >= tau) cm |= 1u << i;
         const int cnt = __popc(cm);
         int incl = cnt;
 #pragma unroll
