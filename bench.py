@@ -297,6 +297,25 @@ def measure_workload(name, dev, stream, flush, peak):
            "combine_us": time_flushed(lambda: b.combine(y, d.tok2row, wts, out=out), stream, flush),
            "algorithmic_bytes": {"dispatch": db, "combine": cb}}
     res["dispatch_plus_combine_us"] = res["dispatch_us"] + res["combine_us"]
+    # What a flushed call's time holds besides its kernels: the event pair itself; the write-back
+    # of the flush's own dirty lines (a 256 MiB read of another buffer after the flush leaves the
+    # L2 holding only clean lines); and the combine as a layer runs it, right after the expert
+    # stage that wrote its input (the L2 flushed before the expert stage).
+    clean = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def read_clean():
+        torch.sum(clean, (0,), dtype=torch.int64, out=sink)
+
+    def comb():
+        b.combine(y, d.tok2row, wts, out=out)
+
+    res["fixed_costs"] = {
+        "events_only_us": time_flushed(lambda: None, stream, flush),
+        "combine_us_clean_l2": time_flushed_after(read_clean, comb, stream, flush),
+        "combine_us_after_expert": time_flushed_after(
+            lambda: b.expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E, out=y), comb, stream, flush)}
+    del clean
     res["frac_of_measured_peak"] = {"dispatch": db / (res["dispatch_us"] * 1e-6) / 1e9 / peak,
                                     "combine": cb / (res["combine_us"] * 1e-6) / 1e9 / peak}
     res["pct_of_8TBs"] = {"dispatch": 100 * db / (res["dispatch_us"] * 1e-6) / 1e9 / NOMINAL_HBM_GBS,
