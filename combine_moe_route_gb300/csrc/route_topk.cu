@@ -19,8 +19,9 @@
 // winner is the largest), exponentials summed by a warp butterfly, one IEEE
 // division.  A warp takes several tokens in turn (with up to 12 logits per
 // lane it loads the next token's logits while it selects the current one's);
-// when E = 32 * NPL is a multiple of 128 and no groups apply, the logits are
-// read 16 bytes at a time, four consecutive experts per lane.
+// when E = 32 * NPL is a multiple of 128, the logits are read 16 bytes at a
+// time, four consecutive experts per lane; with groups that layout serves group
+// sizes that are whole runs of lanes of a 128-expert block or whole blocks.
 #include <atomic>
 
 #include "launch.h"
@@ -84,7 +85,7 @@ __device__ __forceinline__ void load_row(const float *__restrict__ row, int E, i
 // form G contiguous groups; a group scores its largest logit; the M best
 // groups are kept (equal scores: smaller group id) and only their experts
 // stay eligible for the K rounds.
-template <int NPL, bool kVec>   // logits per lane: E <= 32 * NPL
+template <int NPL, bool kVec, bool kVecGroups>   // logits per lane: E <= 32 * NPL
 __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(const float *__restrict__ logits,
                                                                                   int T, int E, int K, int G, int M,
                                                                                   int32_t *__restrict__ topk_idx,
@@ -108,8 +109,8 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
         if (!kPrefetch) load_row<NPL, kVec>(logits + g * (long long)E, E, lane, nxt);
         uint32_t key[NPL];
         uint32_t avail = 0;   // bit i: slot i holds an eligible expert
-        // (the 16-byte-load layout runs only for plain routing over exactly
-        // E = 32 * NPL experts, so there every slot is in range and eligible)
+        // (the 16-byte-load layout runs only over exactly E = 32 * NPL experts,
+        // so there every slot is in range)
 #pragma unroll
         for (int i = 0; i < NPL; ++i) {
             if (kVec || slot_expert<kVec>(lane, i) < E) {
@@ -123,6 +124,53 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
         if (kPrefetch && more) load_row<NPL, kVec>(logits + (g + stride) * (long long)E, E, lane, nxt);
 
         // keep the M best groups; the experts of the others leave the race
+        if constexpr (kVec && kVecGroups) {
+            // 16-byte layout: lane l's slots 4m..4m+3 hold experts 128m + 4l .. +3.
+            // A group of gs < 128 experts is gs/4 consecutive lanes of one
+            // 128-expert block m (gs/4 a power of two); a group of gs >= 128 is
+            // gs/128 whole blocks.  vm[m]: the lane's largest key of block m.
+            const int gs = E / G;
+            uint32_t vm[NPL / 4];
+#pragma unroll
+            for (int m = 0; m < NPL / 4; ++m)
+                vm[m] = max(max(key[4 * m], key[4 * m + 1]), max(key[4 * m + 2], key[4 * m + 3]));
+            uint32_t gkey = 0u;   // lane q < G: the largest key of group q (every real key is > 0)
+            int lpg = 0, gpm = 0, bpg = 0;
+            if (gs < 128) {
+                lpg = gs >> 2;     // lanes per group
+                gpm = 128 / gs;    // groups per block
+#pragma unroll
+                for (int m = 0; m < NPL / 4; ++m)
+                    for (int off = 1; off < lpg; off <<= 1) vm[m] = max(vm[m], __shfl_xor_sync(0xffffffffu, vm[m], off));
+                // group q = m * gpm + s sits in lanes s * lpg .. s * lpg + lpg - 1 of block m
+                const int src = (lane % gpm) * lpg;
+#pragma unroll
+                for (int m = 0; m < NPL / 4; ++m) {
+                    const uint32_t t = __shfl_sync(0xffffffffu, vm[m], src);
+                    if (lane / gpm == m) gkey = t;
+                }
+            } else {
+                bpg = gs >> 7;     // blocks per group
+#pragma unroll
+                for (int m = 0; m < NPL / 4; ++m) {
+                    const uint32_t t = __reduce_max_sync(0xffffffffu, vm[m]);
+                    if (lane == m / bpg) gkey = max(gkey, t);
+                }
+            }
+            bool open = lane < G;
+            uint32_t kept = 0u;
+            for (int r = 0; r < M; ++r) {
+                const uint32_t gmax = __reduce_max_sync(0xffffffffu, open ? gkey : 0u);
+                const uint32_t gwin = __reduce_min_sync(0xffffffffu, (open && gkey == gmax) ? (uint32_t)lane : 0xffffffffu);
+                kept |= 1u << gwin;
+                if ((uint32_t)lane == gwin) open = false;
+            }
+#pragma unroll
+            for (int m = 0; m < NPL / 4; ++m) {
+                const int q = (gs < 128) ? m * gpm + lane / lpg : m / bpg;
+                if (!((kept >> q) & 1u)) avail &= ~(0xfu << (4 * m));
+            }
+        }
         if (!kVec && G > 1) {
             const int gs = E / G;
             // group of slot i, when every slot lies inside one group (group size a
@@ -186,7 +234,7 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
 #pragma unroll
         for (int i = 0; i < NPL; ++i) {
             // the plain top-K keeps every in-range slot; key[i] is already 0 past E
-            ek[i] = (kVec || G <= 1 || (avail & (1u << i))) ? key[i] : 0u;
+            ek[i] = ((kVec && !kVecGroups) || (!kVec && G <= 1) || (avail & (1u << i))) ? key[i] : 0u;
             lmax = max(lmax, ek[i]);
         }
         uint32_t v = lmax ? ((lmax & ~31u) | (uint32_t)(31 - lane)) : 0u;
@@ -288,7 +336,7 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
 // One block per 8 tokens, capped at MOE_ROUTE_WAVES resident waves of blocks
 // when the kernel prefetches (measured on the DeepSeek-V3 prefill logits: 2
 // waves 21.5 us, 1 wave 23.0 us, one token per warp 23.3 us).
-template <int NPL, bool kVec>
+template <int NPL, bool kVec, bool kVecGroups>
 static cudaError_t launch_npl(const float *logits, int T, int E, int K, int G, int M, int32_t *topk_idx,
                               float *topk_w, cudaStream_t stream) {
     static std::atomic<int> per_sm_cache[64];
@@ -298,7 +346,7 @@ static cudaError_t launch_npl(const float *logits, int T, int E, int K, int G, i
     if (dev < 0 || dev >= 64) dev = 0;
     int per_sm = per_sm_cache[dev].load(std::memory_order_relaxed);
     if (per_sm == 0) {
-        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_topk_kernel<NPL, kVec>,
+        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_topk_kernel<NPL, kVec, kVecGroups>,
                                                            RouteShape::kWarps * 32, 0);
         if (ce != cudaSuccess) return ce;
         if (per_sm < 1) per_sm = 1;
@@ -307,7 +355,7 @@ static cudaError_t launch_npl(const float *logits, int T, int E, int K, int G, i
     long long grid = ((long long)T + RouteShape::kWarps - 1) / RouteShape::kWarps;
     const long long cap = (long long)device_sm_count() * per_sm * MOE_ROUTE_WAVES;
     if (NPL <= 12 && grid > cap) grid = cap;
-    route_topk_kernel<NPL, kVec><<<(unsigned)grid, RouteShape::kWarps * 32, 0, stream>>>(logits, T, E, K, G, M,
+    route_topk_kernel<NPL, kVec, kVecGroups><<<(unsigned)grid, RouteShape::kWarps * 32, 0, stream>>>(logits, T, E, K, G, M,
                                                                                          topk_idx, topk_w);
     return cudaGetLastError();
 }
@@ -315,12 +363,19 @@ static cudaError_t launch_npl(const float *logits, int T, int E, int K, int G, i
 template <int NPL>
 static cudaError_t launch_layout(const float *logits, int T, int E, int K, int G, int M, int32_t *topk_idx,
                                  float *topk_w, cudaStream_t stream) {
-    // 16-byte loads: plain routing over exactly 32 * NPL experts, a multiple of 128, aligned rows
+    // 16-byte loads: exactly 32 * NPL experts, a multiple of 128, aligned rows; groups
+    // that are whole lane runs of a 128-expert block (gs/4 lanes, a power of two) or
+    // whole blocks
     if constexpr (NPL % 4 == 0) {
-        if (G <= 1 && E == 32 * NPL && (reinterpret_cast<uintptr_t>(logits) & 15) == 0)
-            return launch_npl<NPL, true>(logits, T, E, K, G, M, topk_idx, topk_w, stream);
+        if (E == 32 * NPL && (reinterpret_cast<uintptr_t>(logits) & 15) == 0) {
+            if (G <= 1) return launch_npl<NPL, true, false>(logits, T, E, K, G, M, topk_idx, topk_w, stream);
+            const int gs = E / G;
+            const bool runs = gs < 128 && gs % 4 == 0 && 128 % gs == 0;
+            if (runs || gs % 128 == 0)
+                return launch_npl<NPL, true, true>(logits, T, E, K, G, M, topk_idx, topk_w, stream);
+        }
     }
-    return launch_npl<NPL, false>(logits, T, E, K, G, M, topk_idx, topk_w, stream);
+    return launch_npl<NPL, false, false>(logits, T, E, K, G, M, topk_idx, topk_w, stream);
 }
 
 cudaError_t launch_route_topk(const float *logits, int T, int E, int K, int G, int M, int32_t *topk_idx,

@@ -158,6 +158,12 @@ def test_workload_end_to_end(case, oracle):
     (384, 8, 32, 3, 2048),     # 32 groups of 12
     (64, 6, 16, 2, 1000),      # 16 groups of 4, K = 6 of the 8 kept experts
     (1024, 32, 32, 32, 256),   # limits
+    # the 16-byte layout's group forms
+    (512, 8, 2, 1, 4096),      # a group is two whole 128-expert blocks
+    (256, 8, 2, 1, 4096),      # a group is one whole block
+    (128, 4, 32, 8, 4096),     # groups of 4: one lane each
+    (256, 8, 16, 8, 4096),     # groups of 16: four lanes
+    (384, 8, 12, 4, 2048),     # groups of 32 over three blocks
 ])
 def test_route_grouped(E, K, G, M, T, gpu, oracle):
     b = _binding()

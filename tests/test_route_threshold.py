@@ -9,7 +9,8 @@ with its low 5 bits replaced by the tag 31 - l (a lane without keys contributes 
 every eligible key >= tau becomes a candidate.  The selection is exact only if the
 candidates hold the whole top K (key descending, equal keys by smaller expert), which is
 what these rows check: random, tie-heavy and denormal rows, and shapes where fewer than
-K lanes hold keys.  The keys are the order-preserving image of fp32 (after adding +0)."""
+K lanes hold keys.  The keys are the order-preserving image of fp32 (after adding +0).
+The last test models how the 16-byte layout forms group maxima for group-limited routing."""
 import numpy as np
 import pytest
 
@@ -73,3 +74,47 @@ def test_random_rows_admit_few_candidates():
         n = [int(((k := _keys(rng.standard_normal(256).astype(np.float32))) >= _tagged_tau(k, 8, vec)).sum())
              for _ in range(400)]
         assert 8 <= min(n) and np.mean(n) < 10 and max(n) <= 64
+
+
+def _vec_group_maxima(keys, G):
+    """The 16-byte layout's group maxima as the route kernel forms them: each lane's maximum
+    over the four slots of a 128-expert block, a butterfly over the gs/4 lanes of a group
+    (gs < 128) or a whole-warp maximum per block (gs >= 128), then lane q holding group q."""
+    E = keys.size
+    NPL, gs = E // 32, E // G
+    slot = np.array([[keys[128 * (i // 4) + 4 * l + i % 4] for i in range(NPL)] for l in range(32)])
+    vm = np.stack([slot[:, 4 * m:4 * m + 4].max(axis=1) for m in range(NPL // 4)], axis=1)
+    gkey = np.zeros(32, np.uint64)
+    if gs < 128:
+        lpg, gpm = gs // 4, 128 // gs
+        off = 1
+        while off < lpg:
+            vm = np.maximum(vm, vm[np.arange(32) ^ off])
+            off <<= 1
+        src = (np.arange(32) % gpm) * lpg
+        for m in range(NPL // 4):
+            t = vm[src, m]
+            take = np.arange(32) // gpm == m
+            gkey[take] = t[take]
+        group_of = lambda l, i: (i // 4) * gpm + l // lpg
+    else:
+        bpg = gs // 128
+        for m in range(NPL // 4):
+            gkey[m // bpg] = max(gkey[m // bpg], vm[:, m].max())
+        group_of = lambda l, i: (i // 4) // bpg
+    return gkey[:G], group_of
+
+
+@pytest.mark.parametrize("E,G", [(E, G) for E in (128, 256, 384, 512, 1024) for G in range(2, 33)
+                                 if E % G == 0 and ((E // G < 128 and (E // G) % 4 == 0 and 128 % (E // G) == 0)
+                                                    or (E // G) % 128 == 0)])
+def test_vec_layout_group_maxima(E, G):
+    """Group maxima and slot groups of the 16-byte layout equal the contiguous groups'."""
+    rng = np.random.default_rng(E * 64 + G)
+    keys = rng.integers(1, 2**32 - 1, size=E, dtype=np.uint64)
+    gkey, group_of = _vec_group_maxima(keys, G)
+    gs = E // G
+    assert np.array_equal(gkey, keys.reshape(G, gs).max(axis=1))
+    for l in range(32):
+        for i in range(E // 32):
+            assert group_of(l, i) == (128 * (i // 4) + 4 * l + i % 4) // gs
