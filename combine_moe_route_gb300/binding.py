@@ -12,6 +12,7 @@ There is no CPU fallback: if the library is missing, loading raises
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -98,9 +99,31 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.moe_get_device_error.restype = i32
         lib.moe_dispatch_noalloc.argtypes = [vp, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.moe_dispatch_noalloc.restype = i32
+        for reader in ("moe_trace_dispatch", "moe_trace_combine"):   # builds with -DMOE_TRACE only
+            try:
+                fn = getattr(lib, reader)
+            except AttributeError:
+                continue
+            fn.argtypes = [i32, vp]
+            fn.restype = i32
         if default:
             _lib = lib
         return lib
+
+
+@contextlib.contextmanager
+def using_library(lib: ctypes.CDLL):
+    """Route the functions below through ``lib`` (another build, from ``load_library(path)``)
+    inside the ``with`` block; the previous library is restored afterwards."""
+    global _lib
+    with _lock:
+        prev = _lib
+        _lib = lib
+    try:
+        yield lib
+    finally:
+        with _lock:
+            _lib = prev
 
 
 def abi_version() -> int:

@@ -22,8 +22,11 @@
 #include <cuda_bf16.h>
 
 #include "launch.h"
+#include "trace.cuh"
 
 namespace moe {
+
+MOE_TRACE_DEFINE()
 
 constexpr int kCombineThreads = 128;
 constexpr int kCombineBatch = 8;   // row loads in flight per chunk
@@ -60,6 +63,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __nv_bfl
     __shared__ float s_w[MOE_MAX_TOPK];
     const int nchunk = H / 8;
     if (kAfterWait) pdl_wait();
+    if (threadIdx.x == 0) MOE_STAMP(kTrCombineStart);
 
     for (long long g = blockIdx.x; g < T; g += gridDim.x) {
         __syncthreads();   // previous token's readers are done with s_row / s_w
@@ -101,6 +105,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __nv_bfl
             }
         }
     }
+#ifdef MOE_TRACE
+    __syncthreads();
+    if (threadIdx.x == 0) MOE_STAMP(kTrCombineEnd);
+#endif
 }
 
 cudaError_t launch_combine(const void *y, const int32_t *tok2row, const float *topk_w, int T, int K, int H,
@@ -435,5 +443,7 @@ cudaError_t launch_combine_partial_recv(const void *partial, const int32_t *topk
                                                                                            E / R, out);
     return cudaGetLastError();
 }
+
+MOE_TRACE_READER(moe_trace_combine)
 
 }  // namespace moe

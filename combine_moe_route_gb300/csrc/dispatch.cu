@@ -54,6 +54,7 @@
 #include <mutex>
 
 #include "launch.h"
+#include "trace.cuh"
 
 // Scatter launch shape (tunable at build time; the defaults are the measured best):
 // warps per block and bulk-copy ring stages per warp.
@@ -70,6 +71,8 @@
 #endif
 
 namespace moe {
+
+MOE_TRACE_DEFINE()
 
 // --------------------------------------------------------------------------
 // 1. tile histogram + stable in-tile ranks
@@ -90,6 +93,7 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
                                                                  int nstatus) {
     extern __shared__ int32_t hist[];   // [kHistWarps][E]
     pdl_launch_dependents();            // the scan may launch; it waits for this grid's writes
+    if (threadIdx.x == 0) MOE_STAMP(kTrHistStart);
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i < (int)(kWsHeader / 4); i += blockDim.x) header[i] = 0;
         for (int i = threadIdx.x; i < nsignal; i += blockDim.x) signal[i] = 0;
@@ -167,6 +171,7 @@ __global__ void __launch_bounds__(kHistThreads) tile_hist_kernel(const int32_t *
             local_rank[i] = (e >= 0) ? my_hist[e] + r_reg[step] : -1;
         }
     }
+    if (threadIdx.x == 0) MOE_STAMP(kTrHistEnd);
 }
 
 // --------------------------------------------------------------------------
@@ -200,14 +205,17 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
     const int lane = tid & 31;
     const int warp = tid >> 5;
 
+    if (tid == 0) MOE_STAMP(kTrScanStart);
     // virtual block id in start order: every lower id has started, so the
     // lookback below only waits on blocks that are already running
     pdl_launch_dependents();   // the scatter may launch and stage its first rows
     pdl_wait();                                    // the tile histogram is complete and visible
+    if (tid == 0) MOE_STAMP(kTrScanWaitDone);
     // ticket and flags were cleared by the histogram grid
     if (tid == 0) s_vid = atomicAdd(ticket, 1);
     __syncthreads();
     const int vid = s_vid;
+    if (tid == 0) MOE_STAMP(kTrScanTicket);
     // warp w owns kScanPerThread consecutive 32-element slices of the block's
     // chunk; slice k is read and written by the 32 lanes together (coalesced)
     const long long wbase = (long long)vid * kScanChunk + (long long)warp * (32 * kScanPerThread);
@@ -230,6 +238,7 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
     }
     if (lane == 0) s_warp[warp] = wsum;
     __syncthreads();
+    if (tid == 0) MOE_STAMP(kTrScanLocal);
     if (warp == 0) {
         const int wv = (lane < kScanThreads / 32) ? s_warp[lane] : 0;
         const int wincl = warp_inclusive_scan(wv);
@@ -275,12 +284,14 @@ __global__ void __launch_bounds__(kScanThreads) lookback_scan_kernel(const int32
         }
     }
     __syncthreads();
+    if (tid == 0) MOE_STAMP(kTrScanLookback);
     const int wexcl = s_excl + s_warp[warp];
 #pragma unroll
     for (int k = 0; k < kScanPerThread; ++k) {
         const long long i = wbase + k * 32 + lane;
         if (i < n) out[i] = wexcl + slice_excl[k] + incl[k] - v[k];
     }
+    if (tid == 0) MOE_STAMP(kTrScanEnd);
 }
 
 // --------------------------------------------------------------------------
@@ -445,6 +456,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
     const long long gw = (long long)blockIdx.x * MOE_SCATTER_WARPS + warp;
     const long long first_dynamic = (long long)S * W;
 
+    if (threadIdx.x == 0) MOE_STAMP(kTrScatterStart);
     // prologue: the source rows do not depend on the histogram or the scan,
     // so the first S tokens are loaded before waiting for it
     int claimed = 0;      // tokens this warp has claimed and started loading
@@ -480,6 +492,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
     // Nothing before this wait touches the workspace header: the unordered
     // low-latency mode zeroes it in the kernel this one waits for.
     pdl_wait();
+    if (lane == 0) MOE_STAMP(kTrScatterWaitDone);
     if (lane == 0) {
         if (failed_at == 0) set_device_error(a.err, MOE_DEVERR_COPY_TIMEOUT);
         if (claimed == S) next_g = first_dynamic + atomicAdd(a.next_token, 1);
@@ -590,6 +603,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
         __syncwarp();
 
         // 4. K bulk stores from the stage
+        if (lane == 0) MOE_STAMP(kTrScatterFirstStore);
         if (lane == 0) {
             for (int j = 0; j < K; ++j) {
                 const int row = s_rows[warp][j];
@@ -632,6 +646,7 @@ __global__ void __launch_bounds__(MOE_SCATTER_WARPS * 32) scatter_kernel(const S
                 (void)mbar_wait_bounded(&bars[warp][t % S], (uint32_t)((t / S) & 1));
         }
         bulk_wait_all();
+        MOE_STAMP(kTrScatterWarpEnd);
         if (send) {
             // the bulk stores are complete; order them before the releases below
             fence_proxy_async_global();
@@ -734,6 +749,7 @@ __host__ __device__ inline size_t small_ids_offset(int W, int stages, int H, boo
 
 __global__ void dispatch_prep_kernel(int32_t *__restrict__ header, int32_t *__restrict__ signal, int nsignal) {
     pdl_launch_dependents();
+    if (threadIdx.x == 0) MOE_STAMP(kTrPrepStart);
     for (int i = threadIdx.x; i < (int)(kWsHeader / 4); i += blockDim.x) header[i] = 0;
     for (int i = threadIdx.x; i < nsignal; i += blockDim.x) signal[i] = 0;
 }
@@ -759,6 +775,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
     const bool send = a.arrive != nullptr;
 
     const long long g0 = (long long)blockIdx.x * a.tpb;
+    if (threadIdx.x == 0) MOE_STAMP(kTrSmallStart);
     const long long g1 = min(g0 + (long long)a.tpb, (long long)T);
     const int ntok = (int)(g1 - g0);
     const int my_n = ntok > warp ? (ntok - warp + W - 1) / W : 0;   // tokens g0 + warp + it*W
@@ -818,6 +835,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
         for (long long i = ids_bulk / 4 + threadIdx.x; i < n_all; i += blockDim.x) s_items[i] = __ldg(a.topk_idx + i);
     }
     staged = __syncthreads_and(staged) != 0;
+    if (threadIdx.x == 0) MOE_STAMP(kTrSmallStaged);
     const int32_t *ids = staged ? s_items : a.topk_idx;
     const long long pb = g0 * K;
     // Each thread takes 16 consecutive items per round and issues all their
@@ -919,6 +937,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
         }
     }
     __syncthreads();
+    if (threadIdx.x == 0) MOE_STAMP(kTrSmallCounted);
 
     // C. start(e): exclusive scan of tot, in place, by the whole block: thread t
     // takes the consecutive entries [t*q, t*q + q) (q = ceil(E / threads), at
@@ -954,6 +973,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
     // ahead; this kernel waits for it (griddepcontrol.wait, a no-op once it has
     // completed) only right before it first writes either -- an error bit, or
     // the send half's announcements at the end -- so the stores never wait.
+    if (threadIdx.x == 0) MOE_STAMP(kTrSmallLayout);
     auto report = [&](int bits) {
         pdl_wait();
         set_device_error(a.err, bits);
@@ -1025,6 +1045,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
             float *sc = reinterpret_cast<float *>(buf + (size_t)H * 2);
             if (kFp8) quantize_stage(buf, H, lane);
             __syncwarp();
+            if (lane == 0) MOE_STAMP(kTrSmallFirstStore);
             if (lane == 0) {
                 for (int j = 0; j < K; ++j) {
                     const int row = s_row[k0 + j];
@@ -1099,6 +1120,7 @@ __global__ void __launch_bounds__(kSmallMaxWarps * 32) dispatch_small_kernel(con
                 (void)mbar_wait_bounded(&bars[warp][t % S], (uint32_t)((t / S) & 1));
         }
         bulk_wait_all();
+        MOE_STAMP(kTrSmallWarpEnd);
         if (send) {
             fence_proxy_async_global();
             __threadfence();
@@ -1556,5 +1578,7 @@ cudaError_t launch_dispatch_ll_unordered(const void *x, const int32_t *topk_idx,
     a.C = C;
     return launch_scatter(a, rt, fp8, kLowLatencyUnordered, stream);
 }
+
+MOE_TRACE_READER(moe_trace_dispatch)
 
 }  // namespace moe
