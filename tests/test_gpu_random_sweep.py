@@ -71,6 +71,24 @@ def _inputs(c):
     return inp
 
 
+def _poisoned(T, H, E, R, K, fp8, dev):
+    """Dispatch outputs filled with values no call writes (NaN rows, e4m3 NaN bytes, -7 maps), so
+    that a row or map entry left unwritten cannot match the oracle by chance."""
+    from combine_moe_route_gb300 import binding as b
+    rows = T * K
+    return b.DispatchResult(
+        recv_x=(torch.full((rows, H), 0x7F, dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn) if fp8
+                else torch.full((rows, H), float("nan"), dtype=torch.bfloat16, device=dev)),
+        recv_scale=torch.full((rows, H // 128), float("nan"), dtype=torch.float32, device=dev) if fp8 else None,
+        counts=torch.full((E * R,), -7, dtype=torch.int32, device=dev),
+        offsets=torch.full((E * R + 1,), -7, dtype=torch.int32, device=dev),
+        expert_offsets=torch.full((E + 1,), -7, dtype=torch.int32, device=dev),
+        tok2row=torch.full((rows,), -7, dtype=torch.int32, device=dev),
+        row2src=torch.full((rows,), -7, dtype=torch.int32, device=dev),
+        workspace=torch.full((max(b.dispatch_workspace_bytes(R, E, K, T), 256),), 0xEE, dtype=torch.uint8,
+                             device=dev))
+
+
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_case(i, gpu, oracle):
     from combine_moe_route_gb300 import binding as b
@@ -98,7 +116,7 @@ def test_random_case(i, gpu, oracle):
     wg = torch.from_numpy(o_w).to(gpu)                # both sides combine with the same weights
 
     # ragged dispatch, expert stand-in, combine
-    d = b.dispatch(x, idx, B, E, fp8=fp8)
+    d = b.dispatch(x, idx, B, E, fp8=fp8, out=_poisoned(T, H, E, R, K, fp8, gpu))
     y = b.expert_scale(d.recv_x, d.recv_scale, d.expert_offsets, E)
     o16 = b.combine(y, d.tok2row, wg)
     o32 = b.combine(y, d.tok2row, wg, out_dtype=torch.float32)
@@ -121,7 +139,8 @@ def test_random_case(i, gpu, oracle):
 
     # split halves: dispatch send (on a random SM budget) -> receive; combine send -> receive
     rng = np.random.default_rng(c["seed"])
-    ds = b.dispatch_send(x, idx, B, E, fp8=fp8, max_sms=int(rng.choice([0, 1, 7, 38])))
+    ds = b.dispatch_send(x, idx, B, E, fp8=fp8, max_sms=int(rng.choice([0, 1, 7, 38])),
+                         out=_poisoned(T, H, E, R, K, fp8, gpu))
     b.dispatch_recv(ds, B, E, K)
     ys = b.expert_scale(ds.recv_x, ds.recv_scale, ds.expert_offsets, E)
     b.combine_send(ds.workspace, R)
