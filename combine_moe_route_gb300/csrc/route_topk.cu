@@ -141,7 +141,8 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
                 gpm = 128 / gs;    // groups per block
 #pragma unroll
                 for (int m = 0; m < NPL / 4; ++m)
-                    for (int off = 1; off < lpg; off <<= 1) vm[m] = max(vm[m], __shfl_xor_sync(0xffffffffu, vm[m], off));
+                    for (int off = 1; off < lpg; off <<= 1)
+                        vm[m] = max(vm[m], __shfl_xor_sync(0xffffffffu, vm[m], off));
                 // group q = m * gpm + s sits in lanes s * lpg .. s * lpg + lpg - 1 of block m
                 const int src = (lane % gpm) * lpg;
 #pragma unroll
@@ -161,7 +162,8 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
             uint32_t kept = 0u;
             for (int r = 0; r < M; ++r) {
                 const uint32_t gmax = __reduce_max_sync(0xffffffffu, open ? gkey : 0u);
-                const uint32_t gwin = __reduce_min_sync(0xffffffffu, (open && gkey == gmax) ? (uint32_t)lane : 0xffffffffu);
+                const uint32_t gwin =
+                    __reduce_min_sync(0xffffffffu, (open && gkey == gmax) ? (uint32_t)lane : 0xffffffffu);
                 kept |= 1u << gwin;
                 if ((uint32_t)lane == gwin) open = false;
             }
@@ -335,7 +337,8 @@ __global__ void __launch_bounds__(RouteShape::kWarps * 32) route_topk_kernel(con
 
 // One block per 8 tokens, capped at MOE_ROUTE_WAVES resident waves of blocks
 // when the kernel prefetches (measured on the DeepSeek-V3 prefill logits: 2
-// waves 21.5 us, 1 wave 23.0 us, one token per warp 23.3 us).
+// waves 19.4 us, 3 waves 19.8 us, 4 waves 20.5 us; on an earlier build 1 wave
+// was 23.0 us and one token per warp 23.3 us against 21.5 us for 2 waves).
 template <int NPL, bool kVec, bool kVecGroups>
 static cudaError_t launch_npl(const float *logits, int T, int E, int K, int G, int M, int32_t *topk_idx,
                               float *topk_w, cudaStream_t stream) {
@@ -355,8 +358,8 @@ static cudaError_t launch_npl(const float *logits, int T, int E, int K, int G, i
     long long grid = ((long long)T + RouteShape::kWarps - 1) / RouteShape::kWarps;
     const long long cap = (long long)device_sm_count() * per_sm * MOE_ROUTE_WAVES;
     if (NPL <= 12 && grid > cap) grid = cap;
-    route_topk_kernel<NPL, kVec, kVecGroups><<<(unsigned)grid, RouteShape::kWarps * 32, 0, stream>>>(logits, T, E, K, G, M,
-                                                                                         topk_idx, topk_w);
+    route_topk_kernel<NPL, kVec, kVecGroups><<<(unsigned)grid, RouteShape::kWarps * 32, 0, stream>>>(
+        logits, T, E, K, G, M, topk_idx, topk_w);
     return cudaGetLastError();
 }
 
